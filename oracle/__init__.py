@@ -1,0 +1,31 @@
+"""CPU oracle for the FlashAttention-2 forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import anything from this package.  The product path
+(``exact_attention_24_gb300``) never imports it and never falls back to it.
+
+The oracle is written from the definition of attention, in float64 NumPy:
+
+* ``attention_ref`` / ``attention_ref_varlen`` -- the plain definition
+  (explicit score matrix, max-shifted softmax, then ``@ V``, then the row
+  log-sum-exp), following "FlashAttention -- for programmers, not
+  researchers." (flash_attention_from_scratch.py), STAGE 1 (softmax) and
+  STAGE 2 (standard attention), plus the scale and the ``L = m + log l``
+  output of "Kernel visualization: Flash Attention 2", sections
+  "Iteration j = 0" (scale after the dot product) and "Write the data back
+  to HBM" (the L array).
+* ``attention_tiled`` -- the tiled online-softmax loop of the same script's
+  STAGE 3 (online softmax) and STAGE 4 (FlashAttention), used to pin the
+  one-pass definition (block-size invariance) and to show that the
+  no-rescale variant of STAGE 4 is wrong.
+
+Every function here is pinned by ``tests/test_oracle.py`` against closed
+forms, brute force in pure Python, and ``torch`` CPU library routines.
+"""
+
+from .attention import (  # noqa: F401
+    attention_ref,
+    attention_ref_varlen,
+    attention_tiled,
+    attention_rows,
+)
