@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the FlashAttention-2 forward pass on GB300.
+
+One step = one forward pass (one kernel launch) over the whole workload:
+B=2, H=16, N=4096, D=128, bf16, causal (the N >= 4096, D = 128 workload on
+which the tensor-peak target is set).  FLOPs = 4 B H N^2 D / 2 (causal).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Inputs are resident in HBM before the timed
+region; they rotate over enough copies that the bytes touched between two
+uses of the same copy exceed the 129 MB L2, so every step starts cold.
+``e2e`` repeats the measurement through the public call with pinned HOST
+buffers, host->device copies of Q, K, V and device->host copies of O, L
+inside the timed region.  ``--impl reference`` times the float64 CPU oracle
+(the only reference implementation there is) on a bounded sample of rows.
+
+Under ``torchrun`` (N > 1) every rank runs its own copy of the workload on
+its own GPU (weak scaling, independent problems, no collective on the data
+path); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, causal & non-causal) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------ distributed --
+def dist_env():
+    """(rank, world, local_rank) from torchrun's environment (1 GPU default)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world > 1
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    """Max of a float over ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own independent problem of the same shape."""
+    return base_seed + 1000 * rank
+
+
+# ------------------------------------------------------------------ peaks --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def load_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source has not changed since it was taken (else None)."""
+    from exact_attention_24_gb300.build import _digest
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(f"{kernel_tag}/{workload}")
+    if not e or e.get("source_digest") != _digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.lines = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        """Median SM clock and the throttle reasons seen in the timed region
+        (between the two marks); all samples if none fell inside it."""
+        if not self.lines:
+            return None
+        if len(self.marks) >= 2:
+            t0, t1 = self.marks[0], self.marks[-1] + 0.15
+            rows = [l for (t, l) in self.lines if t0 <= t <= t1]
+        else:
+            rows = []
+        in_region = bool(rows)
+        rows = rows or [l for _, l in self.lines]
+        sm, smax, reasons = [], [], set()
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "in_timed_region": in_region}
+
+
+def smi_gpu_id(local: int) -> str:
+    """nvidia-smi --id for CUDA device `local` (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+# ------------------------------------------------------------- our arm --
+def bench_ours(args, w, rank, world, local):
+    import torch
+    import exact_attention_24_gb300 as fa
+    from exact_attention_24_gb300.build import build
+    from exact_attention_24_gb300.workloads import Workload, make_inputs
+
+    build()
+    fa.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    wr = Workload(w.name, w.B, w.H, w.N, w.D, w.dtype, w.causal,
+                  rank_seed(w.seed, rank), w.qk_mult, w.lengths)
+    q, k, v = make_inputs(wr)
+    code = fa.FA_BF16
+    in_bytes = 3 * q.numel() * q.element_size()
+    out_b = q.numel() * 2 + q.numel() // w.D * 4
+    copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_b)) + 1)
+    bufs = []
+    with torch.cuda.stream(stream):
+        for _ in range(copies):
+            bufs.append((q.to(dev), k.to(dev), v.to(dev),
+                         torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+                         torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize(dev)
+
+    def launch(i):
+        qd, kd, vd, O, L = bufs[i % copies]
+        st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
+                       code, stream)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd")
+
+    for i in range(args.warmup):
+        launch(i)
+    st = fa.fa_check_device_error(stream)
+    if st != fa.FA_OK:
+        raise fa.FaError(st, "warm-up")
+
+    sampler = ClockSampler(smi_gpu_id(local))
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    ev0.record(stream)
+    for i in range(args.steps):
+        launch(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    barrier(world)
+    sampler.stop()
+    st = fa.fa_check_device_error(stream)
+    if st != fa.FA_OK:
+        raise fa.FaError(st, "timed region")
+    ms_local = ev0.elapsed_time(ev1)
+    ms = reduce_max(ms_local, world, device=dev)
+    per_step_ms = ms / args.steps
+    flops = w.flops()
+    value = world * flops * args.steps / (ms * 1e-3) / 1e12
+    achieved = flops / (ms_local / args.steps * 1e-3) / 1e12
+
+    # ----------------------------------------------------------- e2e
+    e2e_steps = max(3, min(args.steps, 30))
+    qh = q.pin_memory()
+    kh = k.pin_memory()
+    vh = v.pin_memory()
+    oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(q.shape[:-1], dtype=torch.float32).pin_memory()
+    qd, kd, vd, O, L = bufs[0]
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale,
+                           int(w.causal), code, stream)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_fwd")
+            oh.copy_(O, non_blocking=True)
+            lh.copy_(L, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device=dev)
+    barrier(world)
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    peak, _, peak_kind = load_peaks()
+    rec = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per_step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
+                   "flops_per_step": flops,
+                   "l2": f"inputs rotated over {copies} resident copies "
+                         f"({copies * (in_bytes + out_b) / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
+                     "traffic": load_traffic("fa_tc", w.name)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    return rec
+
+
+# --------------------------------------------------------- CPU oracle arm --
+def oracle_rows_sample(w, q, k, v, rows_per_head: int, heads, seed: int):
+    """Rows of the workload for the CPU oracle, and their algorithmic FLOPs."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    picks = []
+    flops = 0.0
+    for (b, h) in heads:
+        rows = np.sort(rng.choice(w.N, size=rows_per_head, replace=False))
+        picks.append((b, h, rows))
+        keys = (rows + 1) if w.causal else np.full(rows.shape, w.N)
+        flops += float(np.sum(4.0 * keys * w.D))
+    return picks, flops
+
+
+def run_oracle_sample(w, qf, kf, vf, picks):
+    from oracle import attention_rows
+    for (b, h, rows) in picks:
+        attention_rows(qf[b, h], kf[b, h], vf[b, h], w.scale, w.causal, rows)
+
+
+def cpu_baseline(w, seconds: float, seed: int = 0):
+    """Time the oracle as it stands on this host's cores, on a bounded sample
+    of the workload's rows (float64, causal keys only)."""
+    import numpy as np
+    from exact_attention_24_gb300.workloads import make_inputs
+    q, k, v = make_inputs(w)
+    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rows = 64
+    done_flops, t_total, n_rows = 0.0, 0.0, 0
+    it = 0
+    while t_total < seconds:
+        picks, fl = oracle_rows_sample(w, qf, kf, vf, rows, [heads[it % len(heads)]], seed + it)
+        t0 = time.perf_counter()
+        run_oracle_sample(w, qf, kf, vf, picks)
+        t_total += time.perf_counter() - t0
+        done_flops += fl
+        n_rows += rows
+        it += 1
+    cores = len(os.sched_getaffinity(0))
+    return {"value": done_flops / t_total / 1e12, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n_rows} query rows ({it} heads x {rows} random rows) of {w.name}, "
+                      f"float64 NumPy, {t_total:.1f} s"}
+
+
+def bench_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    import numpy as np
+    from exact_attention_24_gb300.workloads import make_inputs
+    q, k, v = make_inputs(w)
+    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    # size each step so that warm-up + steps stay within ~90 s
+    picks, _ = oracle_rows_sample(w, qf, kf, vf, 16, heads[:1], 0)
+    t0 = time.perf_counter()
+    run_oracle_sample(w, qf, kf, vf, picks)
+    per_row = max((time.perf_counter() - t0) / 16, 1e-6)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.N, budget / per_row)))
+    for i in range(args.warmup):
+        p, _ = oracle_rows_sample(w, qf, kf, vf, rows, [heads[i % len(heads)]], 10_000 + i)
+        run_oracle_sample(w, qf, kf, vf, p)
+    t_total, fl_total = 0.0, 0.0
+    for i in range(args.steps):
+        p, fl = oracle_rows_sample(w, qf, kf, vf, rows, [heads[i % len(heads)]], i)
+        t0 = time.perf_counter()
+        run_oracle_sample(w, qf, kf, vf, p)
+        t_total += time.perf_counter() - t0
+        fl_total += fl
+    value = fl_total / t_total / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{rows} random query rows of one head per step, {args.steps} steps, "
+              f"of {w.name}; float64 NumPy oracle")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main --
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="B2_H16_N4096_D128_bf16_causal")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from exact_attention_24_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        world = max(world, 1)
+
+    if args.impl == "reference":
+        rec = bench_reference(args, w, rank, world)
+        if rec is not None:
+            print(json.dumps(rec), flush=True)
+        return 0
+
+    import torch
+    init_dist(world, "nccl" if torch.cuda.is_available() else "gloo")
+    rec = bench_ours(args, w, rank, world, local)
+    if rank == 0:
+        if world == 1:
+            rec["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(rec), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,281 @@
+// Device-side helpers shared by the kernels of this library: the bounded
+// mbarrier wait (device watchdog), error reporting, and thin inline-PTX
+// wrappers for mbarrier, TMA (cp.async.bulk.tensor) and tcgen05.
+//
+// Everything here targets sm_103a.  No wait in this library spins without a
+// limit: each one gives up after `limit_ns` of wall time (read from
+// %globaltimer), records FA_ERR_DEVICE_TIMEOUT with the site that gave up in
+// the device error word, raises the CTA's abort flag so the other roles stop
+// too, and returns false.  Nothing here traps.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// ---------------------------------------------------------------- errors --
+__device__ __forceinline__ void record_error(uint32_t *err, uint32_t code,
+                                             uint32_t site) {
+    atomicCAS(err, 0u, FA_ERRWORD(code, site));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------- mbarrier --
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+                 : "memory");
+}
+
+// Make initialised barriers visible to the async proxy (TMA, tcgen05).
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
+                                                      uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+struct WaitCtx {
+    uint32_t *err;               // device error word
+    volatile int *abort_flag;    // CTA-wide abort flag in shared memory
+    uint64_t limit_ns;           // per-wait limit
+};
+
+// Slow path of the bounded wait; kept out of line so the fast path stays a
+// single try_wait in the hot loops.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            const WaitCtx &w, uint32_t site) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0u) {
+            if (*w.abort_flag) return false;
+            // Backstop on the iteration count in case the timer misbehaves.
+            if (globaltimer_ns() - t0 > w.limit_ns || it > (1u << 28)) {
+                record_error(w.err, FA_ERR_DEVICE_TIMEOUT, site);
+                *w.abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait until the phase with parity `parity` of barrier `bar` has completed.
+// Returns false if the wait gave up (timeout, or another role aborted).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const WaitCtx &w, uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, w, site);
+}
+
+// Same, but ignores the abort flag: used at teardown to let copies already
+// in flight land before the CTA exits.
+static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity,
+                                        uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0u &&
+            (globaltimer_ns() - t0 > limit_ns || it > (1u << 28)))
+            return false;
+    }
+}
+
+// ------------------------------------------------------------------ TMA --
+// 3-D tiled bulk tensor load global -> shared, completion counted in bytes
+// on `bar`.  c0 is the innermost (contiguous) coordinate, in elements.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap,
+                                            uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// -------------------------------------------------------------- tcgen05 --
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            dst_smem),
+        "r"(ncols)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
+                                       uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                       uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05 operation this thread issued so
+// far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 32 consecutive columns: thread t of the warp gets lane
+// (taddr.lane + t), columns taddr.col .. +31, into r[0..31].  `r` must point
+// into a register array indexed with compile-time offsets.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+          "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]),
+          "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]),
+          "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]),
+          "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]),
+          "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
+        : "r"(taddr));
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns (store).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+        "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]),
+        "r"(u[13]), "r"(u[14]), "r"(u[15])
+        : "memory");
+}
+
+// 32 lanes x 32 bit, 32 consecutive columns (store) from r[0..31].
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]),
+        "f"(r[7]), "f"(r[8]), "f"(r[9]), "f"(r[10]), "f"(r[11]), "f"(r[12]),
+        "f"(r[13]), "f"(r[14]), "f"(r[15]), "f"(r[16]), "f"(r[17]), "f"(r[18]),
+        "f"(r[19]), "f"(r[20]), "f"(r[21]), "f"(r[22]), "f"(r[23]), "f"(r[24]),
+        "f"(r[25]), "f"(r[26]), "f"(r[27]), "f"(r[28]), "f"(r[29]), "f"(r[30]),
+        "f"(r[31])
+        : "memory");
+}
+
+// --------------------------------------------------------- small numerics --
+// exp2 on the SFU (ex2.approx.ftz.f32): relative error ~2^-22, and
+// exp2(-inf) = +0, which the masking relies on.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Round two floats to bf16 (nearest even) and pack them, `lo` in bits 15..0.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// --------------------------------------------------- varlen bookkeeping --
+// Bounds of sequence `s` from cu_seqlens, validated.  Returns false (and
+// records FA_ERR_INVALID_ARG once) when the entry pair is not a valid
+// non-decreasing range inside [0, total] or longer than max_seqlen.
+__device__ __forceinline__ bool seq_bounds(const int32_t *cu, int s,
+                                           int64_t total, int max_seqlen,
+                                           uint32_t *err, int64_t &start,
+                                           int &len) {
+    const int32_t a = __ldg(cu + s);
+    const int32_t b = __ldg(cu + s + 1);
+    start = a;
+    len = b - a;
+    if (a < 0 || b < a || (int64_t)b > total || len > max_seqlen) {
+        record_error(err, FA_ERR_INVALID_ARG, 0x100u + (uint32_t)(s & 0xff));
+        len = 0;
+        return false;
+    }
+    return true;
+}
+
+}  // namespace fa

@@ -1,0 +1,238 @@
+// C-ABI layer: argument validation, kernel selection, the device error word
+// and the watchdog self-test.  Declarations and contracts live in
+// include/fa.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "fa_internal.h"
+
+// Module-global device error word (see FA_ERRWORD).  Kernels receive its
+// address as a plain pointer so every translation unit can report into it.
+static __device__ uint32_t g_fa_error_word;
+
+namespace {
+
+fa_options g_opts = {FA_KERNEL_AUTO, 0, 0};
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxDevices = 64;
+uint32_t *g_err_addr[kMaxDevices];
+std::mutex g_err_mu;
+
+// Device address of the error word on the current device (looked up once
+// per device; the host-side symbol is not a device address).
+uint32_t *err_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_err_addr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_err_addr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t in_bytes(int dtype) { return dtype == FA_F32 ? 4 : 2; }
+size_t out_bytes(int dtype) { return dtype == FA_BF16 ? 2 : 4; }
+
+// Shared checks of the two entry points.  `tokens` = rows per head summed
+// over the batch (B*N, or total_tokens).
+fa_status check_common(const void *Q, const void *K, const void *V, void *O, float *L,
+                       int64_t heads, int64_t tokens, int D, float scale, int causal,
+                       fa_dtype dtype) {
+    if (D <= 0 || heads < 0 || tokens < 0) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_BF16_OUT_F32)
+        return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (tokens > INT32_MAX || heads > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    const int64_t elems = heads * tokens * D;  // < 2^31 * 2^31 * 128 fits
+    if (elems == 0) return FA_OK;
+    if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(L))
+        return FA_ERR_INVALID_ARG;
+    const size_t ni = (size_t)elems * in_bytes(dtype);
+    const size_t no = (size_t)elems * out_bytes(dtype);
+    const size_t nl = (size_t)(heads * tokens) * sizeof(float);
+    const void *ins[3] = {Q, K, V};
+    for (const void *x : ins)
+        if (overlaps(O, no, x, ni) || overlaps(L, nl, x, ni)) return FA_ERR_INVALID_ARG;
+    if (overlaps(O, no, L, nl)) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+fa_status dispatch(FaProblem &p) {
+    p.err = err_word();
+    if (!p.err) return FA_ERR_CUDA;
+    p.grid_ctas = g_opts.grid_ctas;
+    p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
+    const bool bf16 = p.dtype != FA_F32;
+    switch (g_opts.kernel) {
+        case FA_KERNEL_SIMT: return fa_launch_simt(p);
+        case FA_KERNEL_TC: return bf16 ? fa_launch_tc(p) : FA_ERR_UNSUPPORTED;
+        default: {
+            if (!bf16) return fa_launch_simt(p);
+            const fa_status st = fa_launch_tc(p);
+            return st == FA_ERR_UNSUPPORTED ? fa_launch_simt(p) : st;
+        }
+    }
+}
+
+__global__ void watchdog_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        fa::mbar_init(fa::smem_u32(&bar), 1);
+        fa::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        fa::WaitCtx w{err, &abort_flag, limit_ns};
+        // Nothing arrives on this barrier: the wait must run out and report.
+        (void)fa::mbar_wait(fa::smem_u32(&bar), 0, w, 0xfeu);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t s) {
+    watchdog_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" {
+
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B,
+                 int H, int N, int D, float scale, int causal, fa_dtype dtype,
+                 fa_stream_t stream) {
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    const int64_t heads = (int64_t)B * H;
+    fa_status st = check_common(Q, K, V, O, L, heads, N, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    if (heads == 0 || N == 0) return FA_OK;
+    FaProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.lse = L;
+    p.cu_seqlens = nullptr;
+    p.varlen = 0;
+    p.heads = H;
+    p.units_bh = (int)heads;
+    p.num_seqs = 0;
+    p.n = N;
+    p.total = N;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.dtype = dtype;
+    p.stream = static_cast<cudaStream_t>(stream);
+    return dispatch(p);
+}
+
+fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *L,
+                        const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                        int max_seqlen, int H, int D, float scale, int causal,
+                        fa_dtype dtype, fa_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H < 0)
+        return FA_ERR_INVALID_ARG;
+    fa_status st = check_common(Q, K, V, O, L, H, total_tokens, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    if (num_seqs == 0 || H == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * H > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    FaProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.lse = L;
+    p.cu_seqlens = cu_seqlens;
+    p.varlen = 1;
+    p.heads = H;
+    p.units_bh = num_seqs * H;
+    p.num_seqs = num_seqs;
+    p.n = max_seqlen;
+    p.total = total_tokens;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.dtype = dtype;
+    p.stream = static_cast<cudaStream_t>(stream);
+    return dispatch(p);
+}
+
+fa_status fa_check_device_error(fa_stream_t stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t *err = err_word();
+    if (!err) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    return static_cast<fa_status>(word >> 24);
+}
+
+const char *fa_status_string(fa_status status) {
+    switch (status) {
+        case FA_OK: return "FA_OK: success";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported size or head dimension";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a device-side wait ran past its limit";
+        default: return "unknown fa_status";
+    }
+}
+
+fa_status fa_set_options(const fa_options *opts) {
+    if (!opts) return FA_ERR_INVALID_ARG;
+    if (opts->kernel < FA_KERNEL_AUTO || opts->kernel > FA_KERNEL_TC || opts->grid_ctas < 0)
+        return FA_ERR_INVALID_ARG;
+    g_opts = *opts;
+    return FA_OK;
+}
+
+fa_status fa_get_options(fa_options *opts) {
+    if (!opts) return FA_ERR_INVALID_ARG;
+    *opts = g_opts;
+    return FA_OK;
+}
+
+fa_status fa_watchdog_selftest(uint64_t limit_ns, fa_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return FA_ERR_INVALID_ARG;
+    uint32_t *err = err_word();
+    if (!err) return FA_ERR_CUDA;
+    return fa_launch_watchdog_selftest(err, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Internal host-side interface between the C-ABI layer (fa_api.cu) and the
+// kernel launchers (fa_simt.cu, fa_tc.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+// Device error word layout: bits 31..24 = fa_status code, bits 15..0 = the
+// site that recorded it (first writer wins).
+#define FA_ERRWORD(code, site) ((((uint32_t)(code)) << 24) | ((uint32_t)(site) & 0xffffu))
+
+struct FaProblem {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    float *lse;
+    const int32_t *cu_seqlens;  // null for a dense batch
+    int varlen;
+    int heads;        // H
+    int units_bh;     // dense: B*H; varlen: num_seqs*H
+    int num_seqs;     // varlen only
+    int n;            // dense: N; varlen: max_seqlen
+    int64_t total;    // dense: N (per-head L stride); varlen: total tokens
+    int D;
+    float scale;
+    int causal;
+    int dtype;        // fa_dtype
+    uint32_t *err;    // device error word
+    int grid_ctas;    // 0 = one per SM
+    uint64_t wait_limit_ns;
+    cudaStream_t stream;
+};
+
+fa_status fa_launch_simt(const FaProblem &p);
+fa_status fa_launch_tc(const FaProblem &p);
+fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns,
+                                      cudaStream_t stream);

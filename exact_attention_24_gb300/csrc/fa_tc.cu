@@ -1,0 +1,629 @@
+// Tensor-core (tcgen05 + TMA + TMEM) FlashAttention-2 forward kernel for
+// sm_103a, bf16 inputs, fp32 accumulation.
+//
+// What it computes is the tiled loop of "FlashAttention -- for programmers,
+// not researchers.", STAGE 4 (Q row blocks outside, K/V column blocks
+// inside, running max m / sum l / unnormalised output carried per row, l
+// AND the output rescaled when m moves, one division by l at the end), with
+// the scale applied after the dot product and L = m + ln l written next to O
+// ("Kernel visualization: Flash Attention 2", sections "Iteration j = 0" and
+// "Write the data back to HBM").  Work units are independent (the section
+// "Same operations in another block"), so a persistent grid walks them.
+//
+// How it maps onto GB300 (one CTA per SM, 10 warps):
+//   warps 0-3  softmax for query tile 0 (rows 0..127 of the CTA's block;
+//              TMEM lanes 0..127, one row per thread)
+//   warps 4-7  softmax for query tile 1 (rows 128..255)
+//   warp 8     TMA producer: Q tiles once per block, then K_j, V_j tiles
+//              through an NSLOT-deep ring of shared-memory slots guarded by
+//              full/empty mbarriers
+//   warp 9     TMEM allocator and MMA issuer (one thread):
+//                S_s = Q_s K_j^T          tcgen05.mma, A and B in smem
+//                O_s (+)= P_s V_j         tcgen05.mma, A (=P, bf16) in TMEM
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [256+D, 256+2D).  P_s (bf16, packed 2 per column) overwrites the first
+// 64 columns of S_s after the softmax has read S_s into registers.
+//
+// The two query tiles ping-pong: while the softmax warps of one tile work
+// on S, the tensor core runs the other tile's P V and next Q K^T.
+//
+// Online softmax details (all per row, in registers of the row's thread):
+//   scores stay unscaled; exponentials are exp2(S*c - m*c), c = scale*log2 e
+//   the running max m is only moved (and l, O rescaled) when the new max
+//   exceeds it by more than 8 in log2 units; otherwise the stale m is kept,
+//   which is exact (l and O share the same reference) and bounds P by 2^8.
+//
+// Every mbarrier wait is bounded (device_common.cuh): a stuck pipeline is
+// reported as FA_ERR_DEVICE_TIMEOUT and the CTA drains its copies and MMAs,
+// frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "device_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;             // rows per query tile (MMA M)
+constexpr int BN = 128;             // keys per K/V tile
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int kHalves = D / 64;                    // 128-byte swizzle atoms per row
+    static constexpr int kTileBytes = BN * D * 2;             // one K or V tile (== Q tile)
+    static constexpr int kHalfBytes = BN * 64 * 2;            // 16 KB
+    static constexpr int kSlots = (D == 128) ? 4 : 8;
+    static constexpr int kQBytes = 2 * kTileBytes;
+    static constexpr int kRingOff = kQBytes;
+    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    static constexpr int kBarBytes = 256;
+    // + alignment slack, + 16 KB of padding after the barriers so that no
+    // descriptor-addressed read can leave the CTA's allocation.
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024 + 16384;
+    static_assert(kBarBytes >= 8 * (2 + 2 * kSlots + 6) + 16, "barrier area");
+};
+
+struct TcParams {
+    float *lse;
+    void *o;
+    const int32_t *cu;
+    int varlen;
+    int heads;
+    int units_bh;     // dense: B*H; varlen: num_seqs*H
+    int n;            // dense: N; varlen: max_seqlen
+    int64_t total;    // varlen: total tokens
+    int num_mblk;     // ceil(n / 256)
+    int num_items;    // num_mblk * units_bh
+    float scale;
+    float scale_log2;  // scale * log2(e)
+    int causal;
+    uint32_t *err;
+    uint64_t wait_limit_ns;
+};
+
+// One work item = one 256-row block (two query tiles) of one (b, h) or
+// (sequence, h).  Items are ordered heaviest block first; CTA c takes items
+// c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the ordered list), which pairs
+// heavy and light causal blocks on the same CTA.
+struct Item {
+    int bh;          // dense: b*H + h
+    int h;           // head (varlen coordinates)
+    int64_t start;   // first token of the sequence (varlen), else 0
+    int len;         // rows (= keys) of the sequence
+    int mb;          // 256-row block index
+    int nk0, nk1;    // K/V tiles needed by query tile 0 / 1 (0 = tile empty)
+    int nkv;         // max(nk0, nk1)
+};
+
+__device__ __forceinline__ int snake_item(int round, int cta, int G) {
+    return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+}
+
+// Decode item `idx`; returns false when the item holds no rows.
+__device__ __forceinline__ bool decode_item(const TcParams &p, int idx, Item &it) {
+    const int blk_from_end = idx / p.units_bh;
+    const int u = idx % p.units_bh;
+    it.mb = p.num_mblk - 1 - blk_from_end;
+    if (p.varlen) {
+        const int s = u / p.heads;
+        it.h = u % p.heads;
+        it.bh = 0;
+        int len;
+        int64_t start;
+        if (!seq_bounds(p.cu, s, p.total, p.n, p.err, start, len)) return false;
+        it.start = start;
+        it.len = len;
+    } else {
+        it.bh = u;
+        it.h = 0;
+        it.start = 0;
+        it.len = p.n;
+    }
+    const int row0 = it.mb * 2 * BM;
+    if (row0 >= it.len) return false;
+    const int tiles = (it.len + BN - 1) / BN;
+    if (p.causal) {
+        it.nk0 = min(tiles, 2 * it.mb + 1);
+        it.nk1 = (row0 + BM < it.len) ? min(tiles, 2 * it.mb + 2) : 0;
+    } else {
+        it.nk0 = tiles;
+        it.nk1 = (row0 + BM < it.len) ? tiles : 0;
+    }
+    it.nkv = max(it.nk0, it.nk1);
+    return true;
+}
+
+// ------------------------------------------------ UMMA descriptor helpers --
+// Shared-memory matrix descriptor (tcgen05): start address, leading- and
+// stride-dimension byte offsets (>> 4), fixed version bits 46-47 = 1,
+// swizzle mode 2 (128-byte swizzle) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+           ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), B transposed flag (bit 16: 1 = MN-major), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// S (TMEM, 128 x 128 fp32) = Q (smem, 128 x D) * K^T (smem, 128 x D): both
+// operands K-major with 128-byte swizzle; D/16 MMAs of K = 16.  Within a
+// 64-element swizzle atom the K offset is a plain byte offset (32 B per
+// step); the second half of D=128 is the next 16 KB box.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t kb) {
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32;
+        mma_ss(d_tmem, smem_desc(qa + off, 16, 1024), smem_desc(kb + off, 16, 1024), idesc,
+               kk > 0 ? 1u : 0u);
+    }
+}
+
+// O (TMEM, 128 x D fp32) (+)= P (TMEM, 128 x 128 bf16) * V (smem, 128 x D):
+// V is MN-major (D contiguous) with 128-byte swizzle: 8-key groups are
+// 1024 B apart (SBO), the two 64-column halves of D=128 are 16 KB apart
+// (LBO).  Each MMA consumes 16 keys: 8 TMEM columns of P, 2048 B of V.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint32_t vb,
+                                         bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(BM, D, 1);
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc(vb + kk * 2048, Cfg<D>::kHalfBytes, 1024), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// --------------------------------------------------------------- kernel --
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t q_smem = base;                  // [2][halves][128 rows][128 B]
+    const uint32_t ring = base + C::kRingOff;      // [slots][halves][128][128 B]
+    const uint32_t bars = base + C::kBarOff;
+    // barrier addresses
+    const uint32_t bar_q_full = bars + 0;
+    const uint32_t bar_q_empty = bars + 8;
+    const uint32_t bar_kv_full = bars + 16;                    // [slots]
+    const uint32_t bar_kv_empty = bar_kv_full + 8 * C::kSlots; // [slots]
+    const uint32_t bar_s_full = bar_kv_empty + 8 * C::kSlots;  // [2]
+    const uint32_t bar_p_full = bar_s_full + 16;               // [2]
+    const uint32_t bar_o_final = bar_p_full + 16;              // [2]
+    const uint32_t bar_drain = bar_o_final + 16;
+    uint8_t *gbars = gbase + C::kBarOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + C::kBarBytes - 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + C::kBarBytes - 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == kProducerWarp && lane == 0) {
+        mbar_init(bar_q_full, 1);
+        mbar_init(bar_q_empty, 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(bar_kv_full + 8 * i, 1);
+            mbar_init(bar_kv_empty + 8 * i, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_s_full + 8 * s, 1);
+            mbar_init(bar_p_full + 8 * s, 4);
+            mbar_init(bar_o_final + 8 * s, 1);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t lc = 0;          // K/V loads issued
+            uint32_t items = 0;       // items loaded
+            bool ok = true;
+            for (int k = 0; ok && k * G < p.num_items; ++k) {
+                const int idx = snake_item(k, cta, G);
+                if (idx >= p.num_items) continue;
+                Item it;
+                if (!decode_item(p, idx, it)) continue;
+                if (items > 0 && !mbar_wait(bar_q_empty, (items - 1) & 1, wc, 1)) { ok = false; break; }
+                mbar_arrive_expect_tx(bar_q_full, 2 * C::kTileBytes);
+                for (int s = 0; s < 2; ++s) {
+                    const int row = it.mb * 2 * BM + s * BM;
+                    for (int hf = 0; hf < C::kHalves; ++hf) {
+                        const uint32_t dst = q_smem + s * C::kTileBytes + hf * C::kHalfBytes;
+                        if (p.varlen)
+                            tma_load_3d(dst, &tm_q, bar_q_full, hf * 64, it.h, (int)(it.start + row));
+                        else
+                            tma_load_3d(dst, &tm_q, bar_q_full, hf * 64, row, it.bh);
+                    }
+                }
+                ++items;
+                for (int j = 0; j < it.nkv && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t slot = lc % C::kSlots, round = lc / C::kSlots;
+                        if (round > 0 && !mbar_wait(bar_kv_empty + 8 * slot, (round - 1) & 1, wc, 2)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = bar_kv_full + 8 * slot;
+                        mbar_arrive_expect_tx(fb, C::kTileBytes);
+                        const CUtensorMap *tm = kv == 0 ? &tm_k : &tm_v;
+                        for (int hf = 0; hf < C::kHalves; ++hf) {
+                            const uint32_t dst = ring + slot * C::kTileBytes + hf * C::kHalfBytes;
+                            if (p.varlen)
+                                tma_load_3d(dst, tm, fb, hf * 64, it.h, (int)(it.start + j * BN));
+                            else
+                                tma_load_3d(dst, tm, fb, hf * 64, j * BN, it.bh);
+                        }
+                        ++lc;
+                    }
+                }
+            }
+            // Teardown: let every copy already issued land before exit.
+            const uint64_t lim = p.wait_limit_ns;
+            const uint32_t first = lc > (uint32_t)C::kSlots ? lc - C::kSlots : 0;
+            for (uint32_t i = first; i < lc; ++i)
+                mbar_drain(bar_kv_full + 8 * (i % C::kSlots), (i / C::kSlots) & 1, lim);
+            if (items > 0) mbar_drain(bar_q_full, (items - 1) & 1, lim);
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------- MMA
+        if (lane == 0) {
+            uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0;
+            bool ok = true;
+            for (int k = 0; ok && k * G < p.num_items; ++k) {
+                const int idx = snake_item(k, cta, G);
+                if (idx >= p.num_items) continue;
+                Item it;
+                if (!decode_item(p, idx, it)) continue;
+                if (!mbar_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
+                ++items;
+                tc_fence_after();
+                // K_j and V_j are ring loads number lc + 2j and lc + 2j + 1.
+                const uint32_t l0 = lc;
+                lc += 2 * it.nkv;
+                if (!mbar_wait(bar_kv_full + 8 * ((l0) % C::kSlots), ((l0) / C::kSlots) & 1, wc, 4)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // prologue: S_s = Q_s K_0^T
+                const uint32_t k0 = ring + (l0 % C::kSlots) * C::kTileBytes;
+                issue_qk<D>(tmem + 0 * BN, q_smem, k0);
+                mma_commit(bar_s_full);
+                if (it.nk1 > 0) {
+                    issue_qk<D>(tmem + 1 * BN, q_smem + C::kTileBytes, k0);
+                    mma_commit(bar_s_full + 8);
+                }
+                if (it.nkv == 1) mma_commit(bar_q_empty);
+                for (int j = 0; j < it.nkv; ++j) {
+                    const uint32_t li_k = l0 + 2 * j, li_v = li_k + 1, li_kn = li_k + 2;
+                    if (!mbar_wait(bar_kv_full + 8 * (li_v % C::kSlots), (li_v / C::kSlots) & 1, wc, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vb = ring + (li_v % C::kSlots) * C::kTileBytes;
+                    const uint32_t kn = ring + (li_kn % C::kSlots) * C::kTileBytes;
+                    bool kn_ready = false;
+                    // query tile 0
+                    if (j < it.nk0) {
+                        if (!mbar_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
+                        ++pc0;
+                        tc_fence_after();
+                        issue_pv<D>(tmem + 2 * BN, tmem + 0 * BN, vb, j > 0);
+                        if (j + 1 < it.nk0) {
+                            if (!mbar_wait(bar_kv_full + 8 * (li_kn % C::kSlots), (li_kn / C::kSlots) & 1, wc, 8)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            kn_ready = true;
+                            issue_qk<D>(tmem + 0 * BN, q_smem, kn);
+                            mma_commit(bar_s_full);
+                        } else {
+                            mma_commit(bar_o_final);
+                        }
+                    }
+                    // query tile 1
+                    if (j < it.nk1) {
+                        if (!mbar_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
+                        ++pc1;
+                        tc_fence_after();
+                        issue_pv<D>(tmem + 2 * BN + D, tmem + 1 * BN, vb, j > 0);
+                        if (j + 1 < it.nk1) {
+                            if (!kn_ready) {
+                                if (!mbar_wait(bar_kv_full + 8 * (li_kn % C::kSlots), (li_kn / C::kSlots) & 1, wc, 9)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            issue_qk<D>(tmem + 1 * BN, q_smem + C::kTileBytes, kn);
+                            mma_commit(bar_s_full + 8);
+                        } else {
+                            mma_commit(bar_o_final + 8);
+                        }
+                    }
+                    if (j == it.nkv - 2) mma_commit(bar_q_empty);  // last Q K^T of the item issued
+                    mma_commit(bar_kv_empty + 8 * (li_k % C::kSlots));
+                    mma_commit(bar_kv_empty + 8 * (li_v % C::kSlots));
+                }
+            }
+            // Teardown: wait for every MMA issued so far before TMEM is freed.
+            mma_commit(bar_drain);
+            mbar_drain(bar_drain, 0, p.wait_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int s = warp >> 2;          // query tile of this warpgroup
+        const int quarter = warp & 3;     // TMEM lane quarter
+        const int r = quarter * 32 + lane;  // row within the query tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + s * BN;           // S_s / P_s
+        const uint32_t t_o = tmem + lane_off + 2 * BN + s * D;   // O_s
+        const float c = p.scale_log2;
+        uint32_t sc = 0, oc = 0;  // S_full and O_final phases consumed
+        bool ok = true;
+        for (int k = 0; ok && k * G < p.num_items; ++k) {
+            const int idx = snake_item(k, cta, G);
+            if (idx >= p.num_items) continue;
+            Item it;
+            if (!decode_item(p, idx, it)) continue;
+            const int nks = s == 0 ? it.nk0 : it.nk1;
+            if (nks == 0) continue;
+            const int row = it.mb * 2 * BM + s * BM + r;   // row within the sequence
+            float m_use = -INFINITY, l = 0.f;
+            for (int j = 0; j < nks; ++j) {
+                if (!mbar_wait(bar_s_full + 8 * s, sc & 1, wc, 16 + s)) { ok = false; break; }
+                ++sc;
+                tc_fence_after();
+                float x[BN];
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc)
+                    tmem_ld32(t_s + cc * 32, x + cc * 32);
+                tmem_wait_ld();
+                const int key0 = j * BN;
+                const bool need_mask = (key0 + BN > it.len) || (p.causal && key0 + BN - 1 > row - r);
+                if (need_mask) {
+                    const int lim = p.causal ? min(row + 1, it.len) : it.len;  // keys < lim are live
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (key0 + i >= lim) x[i] = -INFINITY;
+                }
+                float mx = x[0];
+#pragma unroll
+                for (int i = 1; i < BN; ++i) mx = fmaxf(mx, x[i]);
+                const float m_new = fmaxf(m_use, mx);
+                const bool move = (m_new - m_use) * c > kRescaleThreshold;
+                float alpha = 1.f;
+                if (move) {
+                    alpha = (m_use == -INFINITY) ? 0.f : ex2_approx((m_use - m_new) * c);
+                    m_use = m_new;
+                }
+                const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+                float rs = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float e0 = ex2_approx(fmaf(x[cc * 32 + 2 * i], c, -mc));
+                        const float e1 = ex2_approx(fmaf(x[cc * 32 + 2 * i + 1], c, -mc));
+                        rs += e0 + e1;
+                        pk[i] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st16(t_s + cc * 16, pk);
+                }
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+                    // O_s *= alpha (rows that keep their max use alpha = 1).
+                    // PV of the previous tile is complete: S_full of this
+                    // tile was committed after it.
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float o[32];
+                        tmem_ld32(t_o + cc * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(t_o + cc * 32, o);
+                    }
+                }
+                l = alpha * l + rs;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full + 8 * s);
+            }
+            if (!ok) break;
+            // ------------------------------------------------- epilogue
+            if (!mbar_wait(bar_o_final + 8 * s, oc & 1, wc, 18 + s)) { ok = false; break; }
+            ++oc;
+            tc_fence_after();
+            const bool live = l > 0.f;
+            const float inv = live ? 1.f / l : 0.f;
+            const bool store = row < it.len;
+            int64_t orow;
+            if (p.varlen)
+                orow = ((it.start + row) * p.heads + it.h) * (int64_t)D;
+            else
+                orow = ((int64_t)it.bh * p.n + row) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float o[32];
+                tmem_ld32(t_o + cc * 32, o);
+                tmem_wait_ld();
+                if (store) {
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + orow + cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + orow +
+                                                               cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                                pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                                pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                                pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                    }
+                }
+            }
+            tc_fence_before();
+            if (store) {
+                const int64_t li = p.varlen ? (int64_t)it.h * p.total + it.start + row
+                                            : (int64_t)it.bh * p.n + row;
+                p.lse[li] = live ? m_use * p.scale + logf(l) : -INFINITY;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------ host side --
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D map over a bf16 tensor: dims {D, d1, d2} with byte strides {s1, s2};
+// box {64, b1, b2}; 128-byte swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *ptr, int D, uint64_t d1, uint64_t d2, uint64_t s1,
+              uint64_t s2, uint32_t b1, uint32_t b2) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {64, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sms = 0;
+        }
+    }
+    return sms;
+}
+
+template <int D, bool OUT_F32>
+fa_status launch(const FaProblem &pr) {
+    using C = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    const uint64_t es = 2;
+    bool ok;
+    if (pr.varlen) {
+        const uint64_t d1 = pr.heads, d2 = pr.total;
+        const uint64_t s1 = D * es, s2 = (uint64_t)pr.heads * D * es;
+        ok = make_map(&mq, pr.q, D, d1, d2, s1, s2, 1, BN) && make_map(&mk, pr.k, D, d1, d2, s1, s2, 1, BN) &&
+             make_map(&mv, pr.v, D, d1, d2, s1, s2, 1, BN);
+    } else {
+        const uint64_t d1 = pr.n, d2 = pr.units_bh;
+        const uint64_t s1 = D * es, s2 = (uint64_t)pr.n * D * es;
+        ok = make_map(&mq, pr.q, D, d1, d2, s1, s2, BN, 1) && make_map(&mk, pr.k, D, d1, d2, s1, s2, BN, 1) &&
+             make_map(&mv, pr.v, D, d1, d2, s1, s2, BN, 1);
+    }
+    if (!ok) return FA_ERR_CUDA;
+    TcParams p;
+    p.lse = pr.lse;
+    p.o = pr.o;
+    p.cu = pr.cu_seqlens;
+    p.varlen = pr.varlen;
+    p.heads = pr.heads;
+    p.units_bh = pr.units_bh;
+    p.n = pr.n;
+    p.total = pr.total;
+    p.num_mblk = (pr.n + 2 * BM - 1) / (2 * BM);
+    const int64_t items = (int64_t)p.num_mblk * pr.units_bh;
+    if (items > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    p.num_items = (int)items;
+    p.scale = pr.scale;
+    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.causal = pr.causal;
+    p.err = pr.err;
+    p.wait_limit_ns = pr.wait_limit_ns;
+    int grid = pr.grid_ctas > 0 ? pr.grid_ctas : num_sms();
+    if (grid <= 0) return FA_ERR_CUDA;
+    if (grid > p.num_items) grid = p.num_items;
+    auto kern = fa_tc_kernel<D, OUT_F32>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(mq, mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+fa_status fa_launch_tc(const FaProblem &pr) {
+    if (pr.dtype != FA_BF16 && pr.dtype != FA_BF16_OUT_F32) return FA_ERR_UNSUPPORTED;
+    const bool f32 = pr.dtype == FA_BF16_OUT_F32;
+    if (pr.D == 64) return f32 ? fa::launch<64, true>(pr) : fa::launch<64, false>(pr);
+    if (pr.D == 128) return f32 ? fa::launch<128, true>(pr) : fa::launch<128, false>(pr);
+    return FA_ERR_UNSUPPORTED;
+}

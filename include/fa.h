@@ -1,0 +1,185 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The operation (for every batch b and head h, or every packed sequence s
+ * and head h):
+ *
+ *     S = scale * Q K^T                    (scale applied after the dot
+ *                                           product: "Kernel visualization:
+ *                                           Flash Attention 2", section
+ *                                           "Iteration j = 0")
+ *     S[i][j] = -inf  for j > i            (causal only; i, j local to the
+ *                                           sequence)
+ *     O = softmax_rows(S) V                ("FlashAttention -- for
+ *                                           programmers, not researchers.",
+ *                                           STAGE 1 and STAGE 2)
+ *     L[i] = m_i + ln(l_i) = ln sum_j exp(S[i][j])
+ *                                          ("Kernel visualization: Flash
+ *                                           Attention 2", section "Write the
+ *                                           data back to HBM": O and L are
+ *                                           written once; L is what the
+ *                                           backward pass needs)
+ *
+ * computed by streaming K/V tiles through on-chip memory with an online
+ * softmax (same script, STAGE 3 and STAGE 4), never forming the N x N
+ * score matrix in memory.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or synchronises inside fa_fwd /
+ *    fa_fwd_varlen; they only enqueue work on `stream` and return.
+ *  - Tensors are contiguous, row-major, and 16-byte aligned.
+ *  - Q, K, V may alias one another.  O and L must not overlap any input or
+ *    each other.
+ *  - D (head dimension) must be 64 or 128.
+ *  - L is always float32, natural-log units.
+ *  - A row whose keys are all masked (impossible for self-attention with
+ *    the causal mask, since the diagonal is never masked) gets O = 0 and
+ *    L = -inf.
+ *  - Errors are returned as fa_status; nothing is thrown across the ABI.
+ *    Checks that need device data (cu_seqlens contents) and the device
+ *    watchdog report through fa_check_device_error().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* null / misaligned / overlapping pointer,
+                                  negative size, bad dtype, non-finite
+                                  scale, or (device side) cu_seqlens that is
+                                  not non-decreasing within [0, total]     */
+    FA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}; sizes beyond the
+                                  int32 token / TMA coordinate range      */
+    FA_ERR_CUDA = 3,           /* a CUDA runtime or driver call failed
+                                  (launch, tensor-map encoding, sync); the
+                                  runtime's last error is cleared         */
+    FA_ERR_DEVICE_TIMEOUT = 4  /* a device-side wait ran past its limit;
+                                  the kernel gave up and returned cleanly */
+} fa_status;
+
+typedef enum fa_dtype {
+    FA_F32 = 0,          /* Q, K, V, O float32; arithmetic in fp32 FFMA    */
+    FA_BF16 = 1,         /* Q, K, V, O bfloat16; tensor-core contractions
+                            with fp32 accumulation, O rounded to nearest   */
+    FA_BF16_OUT_F32 = 2  /* Q, K, V bfloat16, O float32 (same arithmetic
+                            as FA_BF16 without the final rounding of O)    */
+} fa_dtype;
+
+/* A cudaStream_t.  NULL is the legacy default stream. */
+typedef void *fa_stream_t;
+
+/*
+ * fa_fwd -- dense batch.
+ *
+ *   Q, K, V, O : [B, H, N, D] contiguous (element type per `dtype`)
+ *   L          : [B, H, N] float32
+ *   B, H, N    : >= 0 (any zero makes the call a no-op returning FA_OK)
+ *   D          : 64 or 128
+ *   scale      : finite; multiplies Q K^T (typically 1/sqrt(D))
+ *   causal     : 0 or 1; when 1, key j is masked for query i if j > i
+ *
+ * The work is the set of independent (b, h, query-tile) units of the
+ * "Same operations in another block" section of "Kernel visualization:
+ * Flash Attention 2": no unit needs anything from another.
+ *
+ * Returns FA_OK once the work is enqueued on `stream`.
+ */
+FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O,
+                 float *L, int B, int H, int N, int D, float scale,
+                 int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_varlen -- packed batch of variable-length sequences (self
+ * attention: queries and keys share cu_seqlens).
+ *
+ *   Q, K, V, O   : [total_tokens, H, D] contiguous (token-major packing)
+ *   L            : [H, total_tokens] float32
+ *   cu_seqlens   : DEVICE int32[num_seqs + 1]; cu_seqlens[0] = 0,
+ *                  non-decreasing, cu_seqlens[num_seqs] = total_tokens.
+ *                  Sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1]-1
+ *                  and attends only within itself (causal: local indices).
+ *   max_seqlen   : >= the longest sequence (sizes the launch)
+ *
+ * Zero-length sequences are allowed and produce nothing.  The contents of
+ * cu_seqlens are checked on the device; a violation skips the offending
+ * sequence and is reported by fa_check_device_error() as
+ * FA_ERR_INVALID_ARG.
+ */
+FA_API fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O,
+                        float *L, const int32_t *cu_seqlens, int num_seqs,
+                        int total_tokens, int max_seqlen, int H, int D,
+                        float scale, int causal, fa_dtype dtype,
+                        fa_stream_t stream);
+
+/*
+ * fa_check_device_error -- synchronise `stream`, then return (and clear)
+ * the status recorded by kernels of this library on the current device:
+ * FA_ERR_DEVICE_TIMEOUT if a device wait ran out, FA_ERR_INVALID_ARG if a
+ * cu_seqlens check failed, FA_ERR_CUDA if the synchronisation itself
+ * failed, else FA_OK.  This is the only entry point that blocks.
+ */
+FA_API fa_status fa_check_device_error(fa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+FA_API const char *fa_status_string(fa_status status);
+
+/*
+ * Process-wide knobs for tests and measurement (not thread-safe against
+ * concurrent fa_fwd calls).
+ *
+ *   kernel        : FA_KERNEL_AUTO picks the tensor-core kernel for the
+ *                   bf16 dtypes and the FFMA kernel for FA_F32;
+ *                   FA_KERNEL_SIMT forces the FFMA kernel for every dtype;
+ *                   FA_KERNEL_TC forces the tensor-core kernel (bf16 only,
+ *                   FA_ERR_UNSUPPORTED otherwise).
+ *   grid_ctas     : persistent grid size of the tensor-core kernel; 0 means
+ *                   one CTA per SM.  Results must not depend on it beyond
+ *                   rounding (they are bitwise equal in practice: each
+ *                   output row is computed by exactly one CTA in a fixed
+ *                   order).
+ *   wait_limit_ns : limit of every device-side wait; 0 means 2 s.
+ */
+typedef enum fa_kernel {
+    FA_KERNEL_AUTO = 0,
+    FA_KERNEL_SIMT = 1,
+    FA_KERNEL_TC = 2
+} fa_kernel;
+
+typedef struct fa_options {
+    int32_t kernel;
+    int32_t grid_ctas;
+    uint64_t wait_limit_ns;
+} fa_options;
+
+FA_API fa_status fa_set_options(const fa_options *opts);
+FA_API fa_status fa_get_options(fa_options *opts);
+
+/*
+ * fa_watchdog_selftest -- enqueue one tiny kernel that waits, through the
+ * same bounded-wait routine the attention kernels use, on an mbarrier that
+ * nothing ever arrives on, with a limit of `limit_ns` nanoseconds (must be
+ * in (0, 1e9]).  The wait runs out, the kernel records
+ * FA_ERR_DEVICE_TIMEOUT and returns; the next fa_check_device_error()
+ * reports it and the context stays usable.  Exists so the watchdog can be
+ * tested without faulting or hanging a GPU.
+ */
+FA_API fa_status fa_watchdog_selftest(uint64_t limit_ns, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,144 @@
+"""Host-side checks of the C-ABI library: it loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments before touching CUDA.
+CPU only -- no call here launches a kernel: every call either fails
+validation or (on a machine without a GPU) fails to find a device.  Fake
+addresses are used only in calls that must be rejected before any launch."""
+
+import os
+import re
+
+import pytest
+import torch
+
+import exact_attention_24_gb300 as fa
+from exact_attention_24_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def _declared_symbols():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text)
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert set(declared) >= set(fa.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert fa.fa_status_string(code).startswith("FA_")
+    assert "unknown" in fa.fa_status_string(99)
+
+
+A = 1 << 20          # fake, 16-byte aligned "device" addresses: never touched
+STEP = 1 << 30
+
+
+def _ptrs():
+    return [A + i * STEP for i in range(5)]
+
+
+def test_rejects_unsupported_head_dim(lib):
+    q, k, v, o, l = _ptrs()
+    for D in (32, 96, 256):
+        assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, D, 0.1, 0, fa.FA_BF16, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 0, 0.1, 0, fa.FA_BF16, 0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_rejects_bad_arguments(lib):
+    q, k, v, o, l = _ptrs()
+    bad = fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd(q, k, v, o, l, -1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, -1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, -16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, float("nan"), 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, float("inf"), 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 2, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 0, 7, 0) == bad
+    # null and misaligned pointers
+    assert fa.fa_fwd(0, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, 0, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q + 8, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, l + 4, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    # outputs overlapping inputs or each other
+    assert fa.fa_fwd(q, k, v, q + 64, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd(q, k, v, o, o + 16, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == bad
+    # inputs may alias one another.  The fake pointers would reach a kernel
+    # once validation passes, so this runs only where no GPU exists.
+    if not torch.cuda.is_available():
+        st = fa.fa_fwd(q, q, q, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0)
+        assert st == fa.FA_ERR_CUDA
+
+
+def test_zero_sizes_are_noops(lib):
+    for B, H, N in [(0, 1, 16), (1, 0, 16), (1, 1, 0)]:
+        assert fa.fa_fwd(0, 0, 0, 0, 0, B, H, N, 64, 0.1, 1, fa.FA_BF16, 0) == fa.FA_OK
+    assert fa.fa_fwd_varlen(0, 0, 0, 0, 0, 0, 0, 0, 0, 4, 128, 0.1, 1, fa.FA_BF16, 0) == fa.FA_OK
+
+
+def test_varlen_argument_checks(lib):
+    q, k, v, o, l = _ptrs()
+    cu = A + 5 * STEP
+    bad = fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_varlen(q, k, v, o, l, cu, -1, 100, 50, 2, 64, 0.1, 1, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd_varlen(q, k, v, o, l, cu, 2, -1, 50, 2, 64, 0.1, 1, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd_varlen(q, k, v, o, l, cu, 2, 100, -5, 2, 64, 0.1, 1, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd_varlen(q, k, v, o, l, 0, 2, 100, 50, 2, 64, 0.1, 1, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd_varlen(q, k, v, o, l, cu + 2, 2, 100, 50, 2, 64, 0.1, 1, fa.FA_BF16, 0) == bad
+    assert fa.fa_fwd_varlen(q, k, v, o, l, cu, 2, 100, 50, 2, 80, 0.1, 1, fa.FA_BF16, 0) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_options_roundtrip(lib):
+    before = fa.fa_get_options()
+    try:
+        assert fa.fa_set_options(fa.FA_KERNEL_SIMT, 7, 12345) == fa.FA_OK
+        assert fa.fa_get_options() == {"kernel": 1, "grid_ctas": 7, "wait_limit_ns": 12345}
+        assert fa.fa_set_options(9, 0, 0) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_set_options(0, -1, 0) == fa.FA_ERR_INVALID_ARG
+        # fp32 with the tensor-core kernel forced is unsupported
+        fa.fa_set_options(fa.FA_KERNEL_TC, 0, 0)
+        q, k, v, o, l = _ptrs()
+        assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_F32, 0) in (
+            fa.FA_ERR_UNSUPPORTED, fa.FA_ERR_CUDA)
+    finally:
+        fa.fa_set_options(before["kernel"], before["grid_ctas"], before["wait_limit_ns"])
+
+
+def test_watchdog_limit_checked(lib):
+    assert fa.fa_watchdog_selftest(0, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_watchdog_selftest(2_000_000_000, 0) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_valid_call_without_gpu_fails_loudly(lib):
+    """With no CUDA device the library reports FA_ERR_CUDA; it never computes
+    on the CPU instead."""
+    q, k, v, o, l = _ptrs()
+    assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == fa.FA_ERR_CUDA
+    assert fa.fa_check_device_error(0) == fa.FA_ERR_CUDA
+
+
+def test_product_package_does_not_import_oracle():
+    """The oracle is test infrastructure: nothing in the product package may
+    import or load it."""
+    pkg = os.path.join(ROOT, "exact_attention_24_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle)|oracle/|oracle\.", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not pat.search(text), f

@@ -1,0 +1,282 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs, element by element.
+
+Small problems are compared in full (several tiles plus a ragged tail); the
+five benchmark workloads are compared at full size on sampled rows that the
+oracle computes one by one, in the launch configuration bench.py times
+(default options: tensor-core kernel for bf16, one CTA per SM).
+Every test runs under both kernel selections: ``auto`` (the tensor-core
+kernel for bf16) and ``simt`` (the FFMA kernel for every dtype).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_24_gb300 as fa
+from exact_attention_24_gb300 import build as fa_build
+from exact_attention_24_gb300.workloads import (C1, C2, C3, C4, C5, Workload,
+                                                default_scale, make_inputs)
+from helpers import (assert_close, run_dense, run_varlen, sample_rows, to_f64)
+from oracle import attention_ref, attention_ref_varlen, attention_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+BF16_CODES = (fa.FA_BF16_OUT_F32, fa.FA_BF16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa_build.build()
+    fa.load_library()
+    yield
+    fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+
+
+@pytest.fixture(params=["auto", "simt"])
+def kernel(request):
+    code = fa.FA_KERNEL_AUTO if request.param == "auto" else fa.FA_KERNEL_SIMT
+    assert fa.fa_set_options(code, 0, 0) == fa.FA_OK
+    yield request.param
+    fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+
+
+def _dense_case(B, H, N, D, dtype, causal, seed, qk_mult=1.0):
+    w = Workload("case", B, H, N, D, dtype, causal, seed, qk_mult)
+    q, k, v = make_inputs(w)
+    return w, q, k, v
+
+
+# ---------------------------------------------------------------- small --
+SMALL_SHAPES = [
+    (1, 1, 1, 64), (1, 2, 2, 128), (1, 1, 3, 64), (1, 1, 127, 128),
+    (1, 1, 129, 64), (1, 1, 255, 128), (1, 2, 256, 64), (1, 1, 257, 128),
+    (2, 3, 1000, 64), (2, 3, 1000, 128), (1, 2, 640, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_dense_bf16(kernel, shape, causal):
+    B, H, N, D = shape
+    w, q, k, v = _dense_case(B, H, N, D, "bf16", causal, seed=N + D)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, causal)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for code in BF16_CODES:
+        O, L = run_dense(qd, kd, vd, causal, code, w.scale)
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"{kernel} {shape} c={causal} dt={code}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64), (1, 1, 3, 128), (2, 2, 300, 64),
+                                   (1, 2, 513, 128)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_dense_f32(kernel, shape, causal):
+    B, H, N, D = shape
+    w, q, k, v = _dense_case(B, H, N, D, "f32", causal, seed=7 * N + D)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, causal)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), causal, fa.FA_F32, w.scale)
+    assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_F32, f"{shape} c={causal}")
+
+
+@pytest.mark.parametrize("lengths", [(1, 129, 0, 300), (128, 256, 5), (0, 0, 700),
+                                     (2, 3, 1, 130, 257, 77)], ids=str)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_varlen(kernel, lengths, D, causal):
+    w = Workload("vl", 0, 3, 0, D, "bf16", causal, seed=sum(lengths) + D,
+                 lengths=tuple(lengths))
+    q, k, v = make_inputs(w)
+    cu = w.cu_seqlens
+    ref_o, ref_l = attention_ref_varlen(q, k, v, cu, w.scale, causal)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for code in BF16_CODES:
+        O, L = run_varlen(qd, kd, vd, cu, w.max_seqlen, causal, code, w.scale)
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"{kernel} {lengths} c={causal}")
+
+
+# ------------------------------------------------------- full workloads --
+def test_c1_full(kernel):
+    q, k, v = make_inputs(C1)
+    ref_o, ref_l = attention_ref(q, k, v, C1.scale, C1.causal)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), C1.causal, fa.FA_F32, C1.scale)
+    assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_F32, "C1")
+
+
+def test_c2_full(kernel):
+    q, k, v = make_inputs(C2)
+    ref_o, ref_l = attention_ref(q, k, v, C2.scale, C2.causal)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for code in BF16_CODES:
+        O, L = run_dense(qd, kd, vd, C2.causal, code, C2.scale)
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"C2 dt={code}")
+
+
+@pytest.mark.parametrize("w", [C3, C4], ids=lambda w: w.name)
+def test_full_size_sampled_rows(kernel, w):
+    q, k, v = make_inputs(w)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    outs = {code: run_dense(qd, kd, vd, w.causal, code, w.scale) for code in BF16_CODES}
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for idx, (b, h) in enumerate(heads):
+        rows = sample_rows(w.N, 24, seed=idx)
+        ref_o, ref_l = attention_rows(q[b, h], k[b, h], v[b, h], w.scale, w.causal, rows)
+        for code, (O, L) in outs.items():
+            assert_close(to_f64(O[b, h, rows]), to_f64(L[b, h, rows]), ref_o, ref_l,
+                         code, f"{w.name} b={b} h={h} dt={code}")
+
+
+def test_c5_varlen_sampled_rows(kernel):
+    w = C5
+    q, k, v = make_inputs(w)
+    cu = w.cu_seqlens
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    outs = {code: run_varlen(qd, kd, vd, cu, w.max_seqlen, w.causal, code, w.scale)
+            for code in BF16_CODES}
+    for s in range(len(w.lengths)):
+        a, n = int(cu[s]), int(w.lengths[s])
+        for h in (0, 7, 15):
+            rows = sample_rows(n, 12, seed=100 * s + h)
+            ref_o, ref_l = attention_rows(q[a:a + n, h], k[a:a + n, h], v[a:a + n, h],
+                                          w.scale, w.causal, rows)
+            for code, (O, L) in outs.items():
+                assert_close(to_f64(O[a + rows, h]), to_f64(L[h, a + rows]), ref_o, ref_l,
+                             code, f"C5 seq={s} h={h} dt={code}")
+
+
+# ------------------------------------------------ closed forms on the GPU --
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_zero_query_closed_form(kernel, causal, D):
+    """Q = 0: O = mean of the attended V rows, L = ln(#attended keys)."""
+    N = 300
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn(1, 2, N, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, N, D, generator=g).to(torch.bfloat16)
+    q = torch.zeros_like(k)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), causal, fa.FA_BF16_OUT_F32,
+                     default_scale(D))
+    vf = v.double().numpy()
+    cnt = np.arange(1, N + 1) if causal else np.full(N, N)
+    exp_o = (np.cumsum(vf, axis=2) / np.arange(1, N + 1)[:, None]) if causal else \
+        np.broadcast_to(vf.mean(axis=2, keepdims=True), vf.shape)
+    exp_l = np.broadcast_to(np.log(cnt), (1, 2, N))
+    assert_close(to_f64(O), to_f64(L), exp_o, exp_l, fa.FA_BF16_OUT_F32, "Q=0")
+
+
+def test_overflow_scores_f32(kernel):
+    """The page's DEMO 9 scores (800, 810, 805, 790) must give finite, exact
+    softmax weights on the GPU too (float32 path)."""
+    scores = [800.0, 810.0, 805.0, 790.0]
+    D = 64
+    q = torch.zeros(1, 1, 4, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, 4, D)
+    k[0, 0, :, 0] = torch.tensor(scores)
+    v = torch.zeros(1, 1, 4, D)
+    v[0, 0, :, :4] = torch.eye(4)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), False, fa.FA_F32, 1.0)
+    z = sum(math.exp(s - 810.0) for s in scores)
+    w = np.array([math.exp(s - 810.0) / z for s in scores])
+    exp_o = np.zeros((1, 1, 4, D))
+    exp_o[0, 0, :, :4] = w
+    exp_l = np.full((1, 1, 4), 810.0 + math.log(z))
+    # |L| ~ 810: one float32 ulp there is 2^-14 = 6.1e-5, so the 1e-5 bound
+    # (set for |L| of order 1) is widened by one ulp of the stored value.
+    assert_close(to_f64(O), to_f64(L), exp_o, exp_l, fa.FA_F32, "DEMO 9",
+                 l_extra=float(np.spacing(np.float32(810.0))))
+
+
+def test_overflow_scores_bf16(kernel):
+    """Large scores in bf16 (exactly representable): 800, 808, 804, 792."""
+    scores = [800.0, 808.0, 804.0, 792.0]
+    D = 128
+    q = torch.zeros(1, 1, 4, D, dtype=torch.bfloat16)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, 4, D, dtype=torch.bfloat16)
+    k[0, 0, :, 0] = torch.tensor(scores, dtype=torch.bfloat16)
+    v = torch.zeros(1, 1, 4, D, dtype=torch.bfloat16)
+    v[0, 0, :, :4] = torch.eye(4, dtype=torch.bfloat16)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), False, fa.FA_BF16_OUT_F32, 1.0)
+    z = sum(math.exp(s - 808.0) for s in scores)
+    exp_o = np.zeros((1, 1, 4, D))
+    exp_o[0, 0, :, :4] = [math.exp(s - 808.0) / z for s in scores]
+    exp_l = np.full((1, 1, 4), 808.0 + math.log(z))
+    assert_close(to_f64(O), to_f64(L), exp_o, exp_l, fa.FA_BF16_OUT_F32, "large scores",
+                 l_extra=float(np.spacing(np.float32(808.0))))
+
+
+# ---------------------------------------------------- hygiene / safety --
+def test_outputs_written_only_in_bounds(kernel):
+    """Canary regions around O and L must stay untouched."""
+    B, H, N, D = 1, 2, 333, 128
+    w, q, k, v = _dense_case(B, H, N, D, "bf16", True, seed=3)
+    pad = 4096
+    for code in BF16_CODES:
+        odt = torch.bfloat16 if code == fa.FA_BF16 else torch.float32
+        obuf = torch.full((2 * pad + B * H * N * D,), float("nan"), dtype=odt, device=DEV)
+        lbuf = torch.full((2 * pad + B * H * N,), float("nan"), dtype=torch.float32, device=DEV)
+        o_view = obuf[pad:pad + B * H * N * D]
+        l_view = lbuf[pad:pad + B * H * N]
+        st = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), o_view, l_view, B, H, N, D,
+                       w.scale, 1, code, None)
+        assert st == fa.FA_OK
+        assert fa.fa_check_device_error(None) == fa.FA_OK
+        for buf in (obuf, lbuf):
+            assert torch.isnan(buf[:pad].float()).all() and torch.isnan(buf[-pad:].float()).all()
+        assert torch.isfinite(o_view.float()).all() and torch.isfinite(l_view).all()
+
+
+def test_deterministic(kernel):
+    w, q, k, v = _dense_case(2, 4, 1100, 128, "bf16", True, seed=11)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    O1, L1 = run_dense(qd, kd, vd, True, fa.FA_BF16, w.scale)
+    O2, L2 = run_dense(qd, kd, vd, True, fa.FA_BF16, w.scale)
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+def test_grid_size_does_not_change_results():
+    """The persistent tensor-core kernel gives bitwise the same result for any
+    grid size: each output row is produced by one CTA in a fixed order."""
+    w, q, k, v = _dense_case(1, 5, 1500, 128, "bf16", True, seed=12)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    res = []
+    for grid in (0, 1, 7, 300):
+        fa.fa_set_options(fa.FA_KERNEL_AUTO, grid, 0)
+        res.append(run_dense(qd, kd, vd, True, fa.FA_BF16, w.scale))
+    fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+    for O, L in res[1:]:
+        assert torch.equal(O, res[0][0]) and torch.equal(L, res[0][1])
+
+
+def test_invalid_cu_seqlens_reported_on_device(kernel):
+    """A decreasing cu_seqlens is caught on the device: the sequence is
+    skipped and fa_check_device_error reports FA_ERR_INVALID_ARG."""
+    H, D = 2, 64
+    total = 300
+    q = torch.randn(total, H, D, device=DEV).to(torch.bfloat16)
+    O = torch.zeros(total, H, D, device=DEV, dtype=torch.bfloat16)
+    L = torch.zeros(H, total, device=DEV)
+    cu = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)
+    st = fa.fa_fwd_varlen(q, q, q, O, L, cu, 3, total, 300, H, D, 0.125, 1, fa.FA_BF16, None)
+    assert st == fa.FA_OK
+    assert fa.fa_check_device_error(None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_check_device_error(None) == fa.FA_OK  # cleared
+    # the library is still usable
+    run_varlen(q, q, q, np.array([0, 100, 300]), 200, True, fa.FA_BF16, 0.125)
+
+
+def test_watchdog_timeout_reports_and_recovers():
+    """A wait that nothing satisfies runs out after its limit, is reported as
+    FA_ERR_DEVICE_TIMEOUT, and leaves the context usable."""
+    assert fa.fa_watchdog_selftest(50_000_000, None) == fa.FA_OK
+    assert fa.fa_check_device_error(None) == fa.FA_ERR_DEVICE_TIMEOUT
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    w, q, k, v = _dense_case(1, 1, 200, 64, "bf16", True, seed=1)
+    O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), True, fa.FA_BF16_OUT_F32, w.scale)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, True)
+    assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_BF16_OUT_F32, "after watchdog")
