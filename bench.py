@@ -215,19 +215,27 @@ def bench_ours(args, w, rank, world, local):
     out_b = q.numel() * 2 + q.numel() // w.D * 4
     copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_b)) + 1)
     bufs = []
+    l_shape = (w.H, w.total) if w.varlen else q.shape[:-1]
     with torch.cuda.stream(stream):
+        cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32).to(dev) if w.varlen else None
         for _ in range(copies):
             bufs.append((q.to(dev), k.to(dev), v.to(dev),
                          torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
-                         torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)))
+                         torch.empty(l_shape, dtype=torch.float32, device=dev)))
     torch.cuda.synchronize(dev)
 
-    def launch(i):
-        qd, kd, vd, O, L = bufs[i % copies]
-        st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
-                       code, stream)
+    def call(qd, kd, vd, O, L):
+        if w.varlen:
+            st = fa.fa_fwd_varlen(qd, kd, vd, O, L, cu, len(w.lengths), w.total, w.max_seqlen,
+                                  w.H, w.D, w.scale, int(w.causal), code, stream)
+        else:
+            st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
+                           code, stream)
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
+
+    def launch(i):
+        call(*bufs[i % copies])
 
     for i in range(args.warmup):
         launch(i)
@@ -265,7 +273,7 @@ def bench_ours(args, w, rank, world, local):
     kh = k.pin_memory()
     vh = v.pin_memory()
     oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-    lh = torch.empty(q.shape[:-1], dtype=torch.float32).pin_memory()
+    lh = torch.empty(l_shape, dtype=torch.float32).pin_memory()
     qd, kd, vd, O, L = bufs[0]
 
     def e2e_step():
@@ -273,10 +281,7 @@ def bench_ours(args, w, rank, world, local):
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
-            st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale,
-                           int(w.causal), code, stream)
-            if st != fa.FA_OK:
-                raise fa.FaError(st, "fa_fwd")
+            call(qd, kd, vd, O, L)
             oh.copy_(O, non_blocking=True)
             lh.copy_(L, non_blocking=True)
 
@@ -310,6 +315,7 @@ def bench_ours(args, w, rank, world, local):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
                    "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
+                   "lengths": list(w.lengths) if w.varlen else None,
                    "flops_per_step": flops,
                    "l2": f"inputs rotated over {copies} resident copies "
                          f"({copies * (in_bytes + out_b) / 1e6:.0f} MB > 129 MB L2)",
@@ -330,80 +336,93 @@ def bench_ours(args, w, rank, world, local):
 
 
 # --------------------------------------------------------- CPU oracle arm --
-def oracle_rows_sample(w, q, k, v, rows_per_head: int, heads, seed: int):
-    """Rows of the workload for the CPU oracle, and their algorithmic FLOPs."""
+def head_views(w, qf, kf, vf):
+    """(q, k, v) [n, D] float64 views of every attention problem: each
+    (b, h) of a dense batch, or each (sequence, h) of a packed one."""
+    views = []
+    if w.varlen:
+        cu = w.cu_seqlens
+        for s in range(len(w.lengths)):
+            a, b = int(cu[s]), int(cu[s + 1])
+            for h in range(w.H):
+                views.append((qf[a:b, h], kf[a:b, h], vf[a:b, h]))
+    else:
+        for b in range(w.B):
+            for h in range(w.H):
+                views.append((qf[b, h], kf[b, h], vf[b, h]))
+    return views
+
+
+def oracle_rows_sample(w, view, rows: int, seed: int):
+    """Random query rows of one head view and their algorithmic FLOPs."""
     import numpy as np
+    n = view[0].shape[0]
     rng = np.random.default_rng(seed)
-    picks = []
-    flops = 0.0
-    for (b, h) in heads:
-        rows = np.sort(rng.choice(w.N, size=rows_per_head, replace=False))
-        picks.append((b, h, rows))
-        keys = (rows + 1) if w.causal else np.full(rows.shape, w.N)
-        flops += float(np.sum(4.0 * keys * w.D))
-    return picks, flops
+    picks = np.sort(rng.choice(n, size=min(rows, n), replace=False))
+    keys = (picks + 1) if w.causal else np.full(picks.shape, n)
+    return picks, float(np.sum(4.0 * keys * w.D))
 
 
-def run_oracle_sample(w, qf, kf, vf, picks):
+def run_oracle_sample(w, view, picks):
     from oracle import attention_rows
-    for (b, h, rows) in picks:
-        attention_rows(qf[b, h], kf[b, h], vf[b, h], w.scale, w.causal, rows)
+    attention_rows(view[0], view[1], view[2], w.scale, w.causal, picks)
+
+
+def _f64_views(w):
+    from exact_attention_24_gb300.workloads import make_inputs
+    q, k, v = make_inputs(w)
+    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
+    return head_views(w, qf, kf, vf)
 
 
 def cpu_baseline(w, seconds: float, seed: int = 0):
     """Time the oracle as it stands on this host's cores, on a bounded sample
-    of the workload's rows (float64, causal keys only)."""
-    import numpy as np
-    from exact_attention_24_gb300.workloads import make_inputs
-    q, k, v = make_inputs(w)
-    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
-    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    of the workload's rows (float64; causal rows count only their keys)."""
+    views = _f64_views(w)
     rows = 64
-    done_flops, t_total, n_rows = 0.0, 0.0, 0
-    it = 0
+    done_flops, t_total, n_rows, it = 0.0, 0.0, 0, 0
     while t_total < seconds:
-        picks, fl = oracle_rows_sample(w, qf, kf, vf, rows, [heads[it % len(heads)]], seed + it)
+        view = views[it % len(views)]
+        picks, fl = oracle_rows_sample(w, view, rows, seed + it)
         t0 = time.perf_counter()
-        run_oracle_sample(w, qf, kf, vf, picks)
+        run_oracle_sample(w, view, picks)
         t_total += time.perf_counter() - t0
         done_flops += fl
-        n_rows += rows
+        n_rows += len(picks)
         it += 1
     cores = len(os.sched_getaffinity(0))
     return {"value": done_flops / t_total / 1e12, "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": f"{n_rows} query rows ({it} heads x {rows} random rows) of {w.name}, "
+            "sample": f"{n_rows} query rows ({it} heads x up to {rows} random rows) of {w.name}, "
                       f"float64 NumPy, {t_total:.1f} s"}
 
 
 def bench_reference(args, w, rank, world):
     if rank != 0:
         return None
-    import numpy as np
-    from exact_attention_24_gb300.workloads import make_inputs
-    q, k, v = make_inputs(w)
-    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
-    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    views = _f64_views(w)
     # size each step so that warm-up + steps stay within ~90 s
-    picks, _ = oracle_rows_sample(w, qf, kf, vf, 16, heads[:1], 0)
+    picks, _ = oracle_rows_sample(w, views[0], 16, 0)
     t0 = time.perf_counter()
-    run_oracle_sample(w, qf, kf, vf, picks)
-    per_row = max((time.perf_counter() - t0) / 16, 1e-6)
+    run_oracle_sample(w, views[0], picks)
+    per_row = max((time.perf_counter() - t0) / len(picks), 1e-6)
     budget = 90.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(w.N, budget / per_row)))
+    rows = int(max(1, budget / per_row))
     for i in range(args.warmup):
-        p, _ = oracle_rows_sample(w, qf, kf, vf, rows, [heads[i % len(heads)]], 10_000 + i)
-        run_oracle_sample(w, qf, kf, vf, p)
+        view = views[i % len(views)]
+        p, _ = oracle_rows_sample(w, view, rows, 10_000 + i)
+        run_oracle_sample(w, view, p)
     t_total, fl_total = 0.0, 0.0
     for i in range(args.steps):
-        p, fl = oracle_rows_sample(w, qf, kf, vf, rows, [heads[i % len(heads)]], i)
+        view = views[i % len(views)]
+        p, fl = oracle_rows_sample(w, view, rows, i)
         t0 = time.perf_counter()
-        run_oracle_sample(w, qf, kf, vf, p)
+        run_oracle_sample(w, view, p)
         t_total += time.perf_counter() - t0
         fl_total += fl
     value = fl_total / t_total / 1e12
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{rows} random query rows of one head per step, {args.steps} steps, "
+    sample = (f"up to {rows} random query rows of one head per step, {args.steps} steps, "
               f"of {w.name}; float64 NumPy oracle")
     return {
         "impl": "reference",

@@ -183,6 +183,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
+// One lane of a converged warp (the lowest active lane) returns true.  Used
+// so that a whole warp runs the MMA role's control flow while exactly one
+// thread -- always the same one -- issues tcgen05 operations and commits.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -249,6 +260,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Three-input maximum (one instruction on sm_100-family parts).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // Round two floats to bf16 (nearest even) and pack them, `lo` in bits 15..0.

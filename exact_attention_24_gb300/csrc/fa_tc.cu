@@ -59,14 +59,13 @@ struct Cfg {
     static constexpr int kHalves = D / 64;                    // 128-byte swizzle atoms per row
     static constexpr int kTileBytes = BN * D * 2;             // one K or V tile (== Q tile)
     static constexpr int kHalfBytes = BN * 64 * 2;            // 16 KB
-    static constexpr int kSlots = (D == 128) ? 4 : 8;
+    static constexpr int kSlots = (D == 128) ? 5 : 10;
     static constexpr int kQBytes = 2 * kTileBytes;
     static constexpr int kRingOff = kQBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     static constexpr int kBarBytes = 256;
-    // + alignment slack, + 16 KB of padding after the barriers so that no
-    // descriptor-addressed read can leave the CTA's allocation.
-    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024 + 16384;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(kBarBytes >= 8 * (2 + 2 * kSlots + 6) + 16, "barrier area");
 };
 
@@ -140,6 +139,14 @@ __device__ __forceinline__ bool decode_item(const TcParams &p, int idx, Item &it
     return true;
 }
 
+// Bounded wait by every lane of a warp, with a warp-uniform result (a lane
+// that gave up makes the whole warp give up, so control flow never diverges
+// around elect.sync / __syncwarp).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w,
+                                          uint32_t site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
+}
+
 // ------------------------------------------------ UMMA descriptor helpers --
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and
 // stride-dimension byte offsets (>> 4), fixed version bits 46-47 = 1,
@@ -160,15 +167,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
 // S (TMEM, 128 x 128 fp32) = Q (smem, 128 x D) * K^T (smem, 128 x D): both
 // operands K-major with 128-byte swizzle; D/16 MMAs of K = 16.  Within a
 // 64-element swizzle atom the K offset is a plain byte offset (32 B per
-// step); the second half of D=128 is the next 16 KB box.
+// step); the second half of D=128 is the next 16 KB box.  `dq`, `dk` are the
+// descriptors of the tiles' first byte; the address field sits in the low
+// bits, so an offset is added to the descriptor directly (in 16-byte units,
+// never carrying out of the 14-bit field: shared memory is below 256 KB).
+// The issue sequence is straight-line: the single issuing thread is the
+// tensor core's only feeder, so every cycle spent here is tensor idle time.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t kb) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
     constexpr uint32_t idesc = idesc_bf16(BM, BN, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32;
-        mma_ss(d_tmem, smem_desc(qa + off, 16, 1024), smem_desc(kb + off, 16, 1024), idesc,
-               kk > 0 ? 1u : 0u);
+        const uint64_t off = (uint64_t)(((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32) >> 4);
+        mma_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -177,13 +188,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t 
 // 1024 B apart (SBO), the two 64-column halves of D=128 are 16 KB apart
 // (LBO).  Each MMA consumes 16 keys: 8 TMEM columns of P, 2048 B of V.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint32_t vb,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint64_t dv,
+                                         uint32_t accumulate) {
     constexpr uint32_t idesc = idesc_bf16(BM, D, 1);
+    mma_ts(d_tmem, a_tmem, dv, idesc, accumulate);
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc(vb + kk * 2048, Cfg<D>::kHalfBytes, 1024), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 1; kk < BN / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc, 1u);
 }
 
 // --------------------------------------------------------------- kernel --
@@ -301,92 +312,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
-        if (lane == 0) {
-            uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0;
-            bool ok = true;
-            for (int k = 0; ok && k * G < p.num_items; ++k) {
-                const int idx = snake_item(k, cta, G);
-                if (idx >= p.num_items) continue;
-                Item it;
-                if (!decode_item(p, idx, it)) continue;
-                if (!mbar_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
-                ++items;
-                tc_fence_after();
-                // K_j and V_j are ring loads number lc + 2j and lc + 2j + 1.
-                const uint32_t l0 = lc;
-                lc += 2 * it.nkv;
-                if (!mbar_wait(bar_kv_full + 8 * ((l0) % C::kSlots), ((l0) / C::kSlots) & 1, wc, 4)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // prologue: S_s = Q_s K_0^T
-                const uint32_t k0 = ring + (l0 % C::kSlots) * C::kTileBytes;
-                issue_qk<D>(tmem + 0 * BN, q_smem, k0);
+        // The whole warp runs this role's control flow and waits; one elected
+        // lane issues every tcgen05.mma / commit (always the same lane).
+        const uint64_t dq0 = smem_desc(q_smem, 16, 1024);
+        const uint64_t dq1 = smem_desc(q_smem + C::kTileBytes, 16, 1024);
+        const uint64_t dk_ring = smem_desc(ring, 16, 1024);
+        const uint64_t dv_ring = smem_desc(ring, C::kHalfBytes, 1024);
+        constexpr uint64_t kSlotDesc = C::kTileBytes >> 4;  // one slot in descriptor units
+        const uint32_t t_s0 = tmem, t_s1 = tmem + BN;
+        const uint32_t t_o0 = tmem + 2 * BN, t_o1 = tmem + 2 * BN + D;
+        uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0;
+        bool ok = true;
+        for (int k = 0; ok && k * G < p.num_items; ++k) {
+            const int idx = snake_item(k, cta, G);
+            if (idx >= p.num_items) continue;
+            Item it;
+            if (!decode_item(p, idx, it)) continue;
+            if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
+            ++items;
+            tc_fence_after();
+            // K_j and V_j are ring loads number lc + 2j and lc + 2j + 1.
+            const uint32_t l0 = lc;
+            lc += 2 * it.nkv;
+            const uint32_t s_k0 = l0 % C::kSlots;
+            if (!warp_wait(bar_kv_full + 8 * s_k0, (l0 / C::kSlots) & 1, wc, 4)) { ok = false; break; }
+            tc_fence_after();
+            // prologue: S_s = Q_s K_0^T; K_0 is read only by these, release it.
+            if (elect_one()) {
+                issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);
                 mma_commit(bar_s_full);
                 if (it.nk1 > 0) {
-                    issue_qk<D>(tmem + 1 * BN, q_smem + C::kTileBytes, k0);
+                    issue_qk<D>(t_s1, dq1, dk_ring + s_k0 * kSlotDesc);
                     mma_commit(bar_s_full + 8);
                 }
+                mma_commit(bar_kv_empty + 8 * s_k0);
                 if (it.nkv == 1) mma_commit(bar_q_empty);
-                for (int j = 0; j < it.nkv; ++j) {
-                    const uint32_t li_k = l0 + 2 * j, li_v = li_k + 1, li_kn = li_k + 2;
-                    if (!mbar_wait(bar_kv_full + 8 * (li_v % C::kSlots), (li_v / C::kSlots) & 1, wc, 5)) {
-                        ok = false;
-                        break;
+            }
+            __syncwarp();
+            for (int j = 0; j < it.nkv; ++j) {
+                const uint32_t li_v = l0 + 2 * j + 1, li_kn = li_v + 1;
+                const uint32_t s_v = li_v % C::kSlots, s_kn = li_kn % C::kSlots;
+                if (!warp_wait(bar_kv_full + 8 * s_v, (li_v / C::kSlots) & 1, wc, 5)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dv = dv_ring + s_v * kSlotDesc;
+                const uint64_t dkn = dk_ring + s_kn * kSlotDesc;
+                bool kn_ready = false;
+                // query tile 0: O_0 (+)= P_0 V_j, then S_0 = Q_0 K_{j+1}^T
+                if (j < it.nk0) {
+                    if (!warp_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
+                    ++pc0;
+                    const bool more = j + 1 < it.nk0;
+                    if (more) {
+                        if (!warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 8)) {
+                            ok = false;
+                            break;
+                        }
+                        kn_ready = true;
                     }
                     tc_fence_after();
-                    const uint32_t vb = ring + (li_v % C::kSlots) * C::kTileBytes;
-                    const uint32_t kn = ring + (li_kn % C::kSlots) * C::kTileBytes;
-                    bool kn_ready = false;
-                    // query tile 0
-                    if (j < it.nk0) {
-                        if (!mbar_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
-                        ++pc0;
-                        tc_fence_after();
-                        issue_pv<D>(tmem + 2 * BN, tmem + 0 * BN, vb, j > 0);
-                        if (j + 1 < it.nk0) {
-                            if (!mbar_wait(bar_kv_full + 8 * (li_kn % C::kSlots), (li_kn / C::kSlots) & 1, wc, 8)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            kn_ready = true;
-                            issue_qk<D>(tmem + 0 * BN, q_smem, kn);
+                    if (elect_one()) {
+                        issue_pv<D>(t_o0, t_s0, dv, j > 0 ? 1u : 0u);
+                        if (more) {
+                            issue_qk<D>(t_s0, dq0, dkn);
                             mma_commit(bar_s_full);
                         } else {
                             mma_commit(bar_o_final);
                         }
                     }
-                    // query tile 1
-                    if (j < it.nk1) {
-                        if (!mbar_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
-                        ++pc1;
-                        tc_fence_after();
-                        issue_pv<D>(tmem + 2 * BN + D, tmem + 1 * BN, vb, j > 0);
-                        if (j + 1 < it.nk1) {
-                            if (!kn_ready) {
-                                if (!mbar_wait(bar_kv_full + 8 * (li_kn % C::kSlots), (li_kn / C::kSlots) & 1, wc, 9)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                            }
-                            issue_qk<D>(tmem + 1 * BN, q_smem + C::kTileBytes, kn);
+                    __syncwarp();
+                }
+                // query tile 1
+                if (j < it.nk1) {
+                    if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
+                    ++pc1;
+                    const bool more = j + 1 < it.nk1;
+                    if (more && !kn_ready) {
+                        if (!warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 9)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_pv<D>(t_o1, t_s1, dv, j > 0 ? 1u : 0u);
+                        if (more) {
+                            issue_qk<D>(t_s1, dq1, dkn);
                             mma_commit(bar_s_full + 8);
                         } else {
                             mma_commit(bar_o_final + 8);
                         }
                     }
-                    if (j == it.nkv - 2) mma_commit(bar_q_empty);  // last Q K^T of the item issued
-                    mma_commit(bar_kv_empty + 8 * (li_k % C::kSlots));
-                    mma_commit(bar_kv_empty + 8 * (li_v % C::kSlots));
+                    __syncwarp();
                 }
+                // K_{j+1} has had its last reader (Q_s K_{j+1}^T) issued above and
+                // V_j its last (P_1 V_j): release both slots as soon as those
+                // MMAs complete.  Releasing K one tile ahead of V gives the
+                // producer an extra tile of lead on the next K load.
+                if (elect_one()) {
+                    if (j + 1 < it.nkv) mma_commit(bar_kv_empty + 8 * s_kn);
+                    if (j == it.nkv - 2) mma_commit(bar_q_empty);  // last Q K^T of the item issued
+                    mma_commit(bar_kv_empty + 8 * s_v);
+                }
+                __syncwarp();
             }
-            // Teardown: wait for every MMA issued so far before TMEM is freed.
-            mma_commit(bar_drain);
-            mbar_drain(bar_drain, 0, p.wait_limit_ns);
         }
+        // Teardown: wait for every MMA issued so far before TMEM is freed.
+        if (elect_one()) mma_commit(bar_drain);
+        __syncwarp();
+        mbar_drain(bar_drain, 0, p.wait_limit_ns);
     } else {
         // ------------------------------------------------------- softmax
         const int s = warp >> 2;          // query tile of this warpgroup
@@ -408,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = it.mb * 2 * BM + s * BM + r;   // row within the sequence
             float m_use = -INFINITY, l = 0.f;
             for (int j = 0; j < nks; ++j) {
-                if (!mbar_wait(bar_s_full + 8 * s, sc & 1, wc, 16 + s)) { ok = false; break; }
+                if (!warp_wait(bar_s_full + 8 * s, sc & 1, wc, 16 + s)) { ok = false; break; }
                 ++sc;
                 tc_fence_after();
                 float x[BN];
@@ -424,9 +457,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < BN; ++i)
                         if (key0 + i >= lim) x[i] = -INFINITY;
                 }
-                float mx = x[0];
+                // Row max: 8 independent chains of 3-input max, then a tree.
+                float mx8[8];
 #pragma unroll
-                for (int i = 1; i < BN; ++i) mx = fmaxf(mx, x[i]);
+                for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(x[k], x[8 + k]);
+#pragma unroll
+                for (int t = 2; t < 16; t += 2)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], x[8 * t + k], x[8 * t + 8 + k]);
+                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_use, mx);
                 const bool move = (m_new - m_use) * c > kRescaleThreshold;
                 float alpha = 1.f;
@@ -434,20 +474,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alpha = (m_use == -INFINITY) ? 0.f : ex2_approx((m_use - m_new) * c);
                     m_use = m_new;
                 }
+                // p = exp2(S*c - m*c): packed FFMA2 for the arguments, SFU ex2,
+                // 8 independent partial row sums, bf16x2 packing into TMEM.
                 const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
-                float rs = 0.f;
+                const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+                float2 rs4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int cc = 0; cc < BN / 32; ++cc) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float e0 = ex2_approx(fmaf(x[cc * 32 + 2 * i], c, -mc));
-                        const float e1 = ex2_approx(fmaf(x[cc * 32 + 2 * i + 1], c, -mc));
-                        rs += e0 + e1;
-                        pk[i] = pack_bf16x2(e0, e1);
+                        const float2 a = __ffma2_rn(make_float2(x[cc * 32 + 2 * i], x[cc * 32 + 2 * i + 1]),
+                                                    c2, nmc2);
+                        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                        rs4[i & 3] = __fadd2_rn(rs4[i & 3], e);
+                        pk[i] = pack_bf16x2(e.x, e.y);
                     }
                     tmem_st16(t_s + cc * 16, pk);
                 }
+                const float rs = ((rs4[0].x + rs4[0].y) + (rs4[1].x + rs4[1].y)) +
+                                 ((rs4[2].x + rs4[2].y) + (rs4[3].x + rs4[3].y));
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
                     // O_s *= alpha (rows that keep their max use alpha = 1).
                     // PV of the previous tile is complete: S_full of this
@@ -470,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ------------------------------------------------- epilogue
-            if (!mbar_wait(bar_o_final + 8 * s, oc & 1, wc, 18 + s)) { ok = false; break; }
+            if (!warp_wait(bar_o_final + 8 * s, oc & 1, wc, 18 + s)) { ok = false; break; }
             ++oc;
             tc_fence_after();
             const bool live = l > 0.f;
