@@ -27,7 +27,7 @@ __all__ = [
     "FA_ERR_DEVICE_TIMEOUT", "FA_F32", "FA_BF16", "FA_BF16_OUT_F32",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_TC", "FaError",
     "load_library", "library_path", "fa_fwd", "fa_fwd_varlen",
-    "fa_check_device_error", "fa_status_string", "fa_set_options",
+    "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
     "attention_varlen", "EXPORTED_SYMBOLS",
 ]
@@ -38,8 +38,8 @@ FA_F32, FA_BF16, FA_BF16_OUT_F32 = 0, 1, 2
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_check_device_error",
-                    "fa_status_string", "fa_set_options", "fa_get_options",
-                    "fa_watchdog_selftest")
+                    "fa_status_string", "fa_last_cuda_error", "fa_set_options",
+                    "fa_get_options", "fa_watchdog_selftest")
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -48,8 +48,10 @@ _lib = None
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
-        super().__init__(f"{what}: {fa_status_string(status)}" if what else
-                         fa_status_string(status))
+        msg = fa_status_string(status)
+        if status == FA_ERR_CUDA:
+            msg += f" ({fa_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}" if what else msg)
 
 
 class _Options(ctypes.Structure):
@@ -86,6 +88,8 @@ def load_library():
     lib.fa_check_device_error.restype = i32
     lib.fa_status_string.argtypes = [i32]
     lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_cuda_error.argtypes = []
+    lib.fa_last_cuda_error.restype = ctypes.c_char_p
     lib.fa_set_options.argtypes = [ctypes.POINTER(_Options)]
     lib.fa_set_options.restype = i32
     lib.fa_get_options.argtypes = [ctypes.POINTER(_Options)]
@@ -115,6 +119,10 @@ def _stream(s) -> int:
 
 def fa_status_string(status: int) -> str:
     return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_last_cuda_error() -> str:
+    return load_library().fa_last_cuda_error().decode()
 
 
 def fa_fwd(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, stream=None) -> int:

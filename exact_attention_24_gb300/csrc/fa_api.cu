@@ -27,15 +27,17 @@ std::mutex g_err_mu;
 // per device; the host-side symbol is not a device address).
 uint32_t *err_word() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
         return nullptr;
     }
     std::lock_guard<std::mutex> lk(g_err_mu);
     if (!g_err_addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) {
-            cudaGetLastError();
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_error_word);
+        if (e != cudaSuccess) {
+            fa_cuda_fail(e);
             return nullptr;
         }
         g_err_addr[dev] = static_cast<uint32_t *>(p);
@@ -116,9 +118,18 @@ __global__ void watchdog_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
 
 }  // namespace
 
+static thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+fa_status fa_cuda_fail(cudaError_t e) {
+    t_last_cuda_error = e;
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+}
+
 fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t s) {
     watchdog_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
 extern "C" {
@@ -189,19 +200,17 @@ fa_status fa_check_device_error(fa_stream_t stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t *err = err_word();
     if (!err) return FA_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
     uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
+    if ((e = cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return fa_cuda_fail(e);
     return static_cast<fa_status>(word >> 24);
 }
+
+const char *fa_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char *fa_status_string(fa_status status) {
     switch (status) {

@@ -34,6 +34,11 @@ struct FaProblem {
     cudaStream_t stream;
 };
 
+// Record `e` as the calling thread's last CUDA failure (see
+// fa_last_cuda_error) and clear the runtime's sticky-free last error.
+// Returns FA_ERR_CUDA so launchers can `return fa_cuda_fail(e);`.
+fa_status fa_cuda_fail(cudaError_t e);
+
 fa_status fa_launch_simt(const FaProblem &p);
 fa_status fa_launch_tc(const FaProblem &p);
 fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns,

@@ -205,16 +205,13 @@ fa_status launch(const FaProblem &pr) {
     p.err = pr.err;
     const size_t smem = sizeof(float) * (size_t)(kBr * D + kBc * (D + 1) + kBc * D);
     auto kern = fa_simt_kernel<D, Tin, Tout>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
     const int tiles = (pr.n + kBr - 1) / kBr;
     dim3 grid(pr.units_bh, tiles);
     kern<<<grid, kWarps * 32, smem, pr.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
+    e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
 template <int D>

@@ -199,6 +199,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint6
 
 // --------------------------------------------------------------- kernel --
 template <int D, bool OUT_F32>
+// 10 warps put 3 warps on two of the four SM sub-partitions, whose register
+// files hold 16K registers each: at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
     fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -574,10 +576,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     if (!fn) {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
+            fa_cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
             return nullptr;
         }
         fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
@@ -598,7 +600,11 @@ bool make_map(CUtensorMap *m, const void *ptr, int D, uint64_t d1, uint64_t d2, 
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) {
+        fa_cuda_fail(cudaErrorInvalidValue);
+        return false;
+    }
+    return true;
 }
 
 int num_sms() {
@@ -606,8 +612,9 @@ int num_sms() {
     if (!sms) {
         int dev = 0;
         cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
+        const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            fa_cuda_fail(e);
             sms = 0;
         }
     }
@@ -631,7 +638,7 @@ fa_status launch(const FaProblem &pr) {
         ok = make_map(&mq, pr.q, D, d1, d2, s1, s2, BN, 1) && make_map(&mk, pr.k, D, d1, d2, s1, s2, BN, 1) &&
              make_map(&mv, pr.v, D, d1, d2, s1, s2, BN, 1);
     }
-    if (!ok) return FA_ERR_CUDA;
+    if (!ok) return FA_ERR_CUDA;  // reason recorded by make_map
     TcParams p;
     p.lse = pr.lse;
     p.o = pr.o;
@@ -654,14 +661,15 @@ fa_status launch(const FaProblem &pr) {
     if (grid <= 0) return FA_ERR_CUDA;
     if (grid > p.num_items) grid = p.num_items;
     auto kern = fa_tc_kernel<D, OUT_F32>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
+    cudaFuncAttributes fattr;
+    cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    if (fattr.maxThreadsPerBlock < kThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
     kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(mq, mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
+    e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
 }  // namespace

@@ -137,6 +137,14 @@ FA_API fa_status fa_check_device_error(fa_stream_t stream);
 FA_API const char *fa_status_string(fa_status status);
 
 /*
+ * fa_last_cuda_error -- after a call returned FA_ERR_CUDA, the CUDA runtime's
+ * description of the failure (for example "too many resources requested for
+ * launch"), recorded per calling thread; "no error" if none was recorded.
+ * The string is static storage of the CUDA runtime.
+ */
+FA_API const char *fa_last_cuda_error(void);
+
+/*
  * Process-wide knobs for tests and measurement (not thread-safe against
  * concurrent fa_fwd calls).
  *

@@ -38,7 +38,7 @@ def run_dense(q, k, v, causal, code, scale, stream=None):
     O = torch.full((B, H, N, D), float("nan"), dtype=out_dtype(code), device=q.device)
     L = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
     st = fa.fa_fwd(q, k, v, O, L, B, H, N, D, scale, int(causal), code, stream)
-    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
     st = fa.fa_check_device_error(stream)
     assert st == fa.FA_OK, fa.fa_status_string(st)
     return O, L

@@ -129,6 +129,7 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     on the CPU instead."""
     q, k, v, o, l = _ptrs()
     assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_BF16, 0) == fa.FA_ERR_CUDA
+    assert fa.fa_last_cuda_error() != "no error"   # the runtime's reason is kept
     assert fa.fa_check_device_error(0) == fa.FA_ERR_CUDA
 
 
