@@ -224,8 +224,17 @@ def bench_ours(args, w, rank, world, local):
                          torch.empty(l_shape, dtype=torch.float32, device=dev)))
     torch.cuda.synchronize(dev)
 
+    ws = None
+    ws_bytes = 0
+    if args.splits is not None:
+        ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.D, args.splits)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
     def call(qd, kd, vd, O, L):
-        if w.varlen:
+        if args.splits is not None:
+            st = fa.fa_fwd_splitkv(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
+                                   code, args.splits, ws, ws_bytes, stream)
+        elif w.varlen:
             st = fa.fa_fwd_varlen(qd, kd, vd, O, L, cu, len(w.lengths), w.total, w.max_seqlen,
                                   w.H, w.D, w.scale, int(w.causal), code, stream)
         else:
@@ -316,6 +325,7 @@ def bench_ours(args, w, rank, world, local):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
                    "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
                    "lengths": list(w.lengths) if w.varlen else None,
+                   "splits": args.splits,
                    "flops_per_step": flops,
                    "l2": f"inputs rotated over {copies} resident copies "
                          f"({copies * (in_bytes + out_b) / 1e6:.0f} MB > 129 MB L2)",
@@ -329,7 +339,7 @@ def bench_ours(args, w, rank, world, local):
                 "h2d_bytes_per_step": in_bytes,
                 "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.splits not in (None, 1) and ws_bytes else 1),
         "clocks": sampler.summary(),
     }
     return rec
@@ -448,6 +458,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="B2_H16_N4096_D128_bf16_causal")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--splits", type=int, default=None,
+                    help="time fa_fwd_splitkv with this many key splits (0 = automatic)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -26,7 +26,8 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
     "FA_ERR_DEVICE_TIMEOUT", "FA_F32", "FA_BF16", "FA_BF16_OUT_F32",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_TC", "FaError",
-    "load_library", "library_path", "fa_fwd", "fa_fwd_varlen",
+    "load_library", "library_path", "fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
+    "fa_fwd_splitkv_workspace_size",
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
     "attention_varlen", "EXPORTED_SYMBOLS",
@@ -37,7 +38,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, \
 FA_F32, FA_BF16, FA_BF16_OUT_F32 = 0, 1, 2
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_check_device_error",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
+                    "fa_fwd_splitkv_workspace_size", "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
                     "fa_get_options", "fa_watchdog_selftest")
 
@@ -84,6 +86,11 @@ def load_library():
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                   i32, f32, i32, i32, vp]
     lib.fa_fwd_varlen.restype = i32
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                   i32, i32, i32, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_splitkv.restype = i32
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -139,6 +146,19 @@ def fa_fwd_varlen(Q, K, V, O, L, cu_seqlens, num_seqs, total_tokens,
         float(scale), int(causal), int(dtype), _stream(stream))
 
 
+def fa_fwd_splitkv(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, num_splits,
+                   workspace, workspace_bytes, stream=None) -> int:
+    return load_library().fa_fwd_splitkv(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), int(B), int(H), int(N), int(D),
+        float(scale), int(causal), int(dtype), int(num_splits), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, D, num_splits) -> int:
+    return int(load_library().fa_fwd_splitkv_workspace_size(int(B), int(H), int(N), int(D),
+                                                            int(num_splits)))
+
+
 def fa_check_device_error(stream=None) -> int:
     return load_library().fa_check_device_error(_stream(stream))
 
@@ -177,8 +197,11 @@ def _dtype_code(q, out_dtype):
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None,
-              out_dtype=None, stream=None):
-    """O, L for ``[B, H, N, D]`` CUDA tensors (contiguous, same dtype)."""
+              out_dtype=None, stream=None, num_splits: int | None = None):
+    """O, L for ``[B, H, N, D]`` CUDA tensors (contiguous, same dtype).
+
+    ``num_splits`` (bf16 only) selects the split-key path: an int >= 1, or 0
+    for the automatic choice; the workspace is allocated here with torch."""
     import torch
     B, H, N, D = q.shape
     code, odt = _dtype_code(q, out_dtype)
@@ -186,9 +209,15 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None,
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
     O = torch.empty((B, H, N, D), dtype=odt, device=q.device)
     L = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    st = fa_fwd(q, k, v, O, L, B, H, N, D, scale, int(causal), code, stream)
+    if num_splits is None:
+        st = fa_fwd(q, k, v, O, L, B, H, N, D, scale, int(causal), code, stream)
+    else:
+        nbytes = fa_fwd_splitkv_workspace_size(B, H, N, D, num_splits)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_splitkv(q, k, v, O, L, B, H, N, D, scale, int(causal), code,
+                            num_splits, ws, nbytes, stream)
     if st != FA_OK:
-        raise FaError(st, "fa_fwd")
+        raise FaError(st, "fa_fwd" if num_splits is None else "fa_fwd_splitkv")
     return O, L
 
 

@@ -196,6 +196,64 @@ fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, fl
     return dispatch(p);
 }
 
+fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *L, int B,
+                         int H, int N, int D, float scale, int causal, fa_dtype dtype,
+                         int num_splits, void *workspace, size_t workspace_bytes,
+                         fa_stream_t stream) {
+    if (B < 0 || H < 0 || N < 0 || num_splits < 0 || num_splits > 64) return FA_ERR_INVALID_ARG;
+    const int64_t heads = (int64_t)B * H;
+    fa_status st = check_common(Q, K, V, O, L, heads, N, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+    if (heads == 0 || N == 0) return FA_OK;
+    int splits = 1;
+    size_t need = 0;
+    if (!fa_tc_split_plan((int)heads, N, D, num_splits, splits, need)) return FA_ERR_CUDA;
+    if (splits > 1) {
+        if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+        const void *ins[3] = {Q, K, V};
+        const size_t ni = (size_t)heads * N * D * in_bytes(dtype);
+        for (const void *x : ins)
+            if (overlaps(workspace, need, x, ni)) return FA_ERR_INVALID_ARG;
+        if (overlaps(workspace, need, O, (size_t)heads * N * D * out_bytes(dtype)) ||
+            overlaps(workspace, need, L, (size_t)heads * N * sizeof(float)))
+            return FA_ERR_INVALID_ARG;
+    }
+    FaProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.lse = L;
+    p.heads = H;
+    p.units_bh = (int)heads;
+    p.n = N;
+    p.total = N;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.dtype = dtype;
+    p.num_splits = splits;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes;
+    p.stream = static_cast<cudaStream_t>(stream);
+    p.err = err_word();
+    if (!p.err) return FA_ERR_CUDA;
+    p.grid_ctas = g_opts.grid_ctas;
+    p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
+    return fa_launch_tc(p);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int D, int num_splits) {
+    if (B <= 0 || H <= 0 || N <= 0 || (D != 64 && D != 128) || num_splits < 0 || num_splits > 64)
+        return 0;
+    if ((int64_t)B * H > INT32_MAX) return 0;
+    int splits = 1;
+    size_t need = 0;
+    if (!fa_tc_split_plan(B * H, N, D, num_splits, splits, need)) return 0;
+    return need;
+}
+
 fa_status fa_check_device_error(fa_stream_t stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t *err = err_word();

@@ -31,6 +31,9 @@ struct FaProblem {
     uint32_t *err;    // device error word
     int grid_ctas;    // 0 = one per SM
     uint64_t wait_limit_ns;
+    int num_splits;   // split-key mode when > 1 (dense bf16 only)
+    void *workspace;  // split-key partials (caller-owned device memory)
+    size_t workspace_bytes;
     cudaStream_t stream;
 };
 
@@ -41,5 +44,11 @@ fa_status fa_cuda_fail(cudaError_t e);
 
 fa_status fa_launch_simt(const FaProblem &p);
 fa_status fa_launch_tc(const FaProblem &p);
+
+// Split-key planning for the tensor-core kernel: the number of key-range
+// splits used for `requested` (0 = automatic: enough work items to cover the
+// SMs) and the workspace bytes they need.  Returns false if the device
+// cannot be queried.
+bool fa_tc_split_plan(int units_bh, int n, int D, int requested, int &splits, size_t &bytes);
 fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns,
                                       cudaStream_t stream);

@@ -53,6 +53,10 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Epilogue destinations.
+constexpr int kOutBf16 = 0;   // O bf16, L
+constexpr int kOutF32 = 1;    // O fp32, L
+constexpr int kOutPart = 2;   // split-key partial: O_g fp32 and L_g into the workspace
 
 template <int D>
 struct Cfg {
@@ -79,7 +83,10 @@ struct TcParams {
     int n;            // dense: N; varlen: max_seqlen
     int64_t total;    // varlen: total tokens
     int num_mblk;     // ceil(n / 256)
-    int num_items;    // num_mblk * units_bh
+    int num_splits;   // key-range splits per block (1 = none)
+    int num_items;    // num_mblk * num_splits * units_bh
+    float *ws_o;      // split mode: partial O, fp32 [splits][units][n][D]
+    float *ws_l;      // split mode: partial L, fp32 [splits][units][n]
     float scale;
     float scale_log2;  // scale * log2(e)
     int causal;
@@ -97,18 +104,54 @@ struct Item {
     int64_t start;   // first token of the sequence (varlen), else 0
     int len;         // rows (= keys) of the sequence
     int mb;          // 256-row block index
-    int nk0, nk1;    // K/V tiles needed by query tile 0 / 1 (0 = tile empty)
+    int g;           // key-range split of the block
+    int t0;          // first K/V tile of the split
+    int nk0, nk1;    // K/V tiles (from t0) needed by query tile 0 / 1 (0 = none)
     int nkv;         // max(nk0, nk1)
 };
+
+// K/V tile range of split g of a block whose two query tiles need nk0_full and
+// nk1_full tiles from tile 0: the block's nkv tiles are cut into num_splits
+// contiguous, near-equal ranges.  Shared by the kernel and the merge.
+__host__ __device__ __forceinline__ void split_range(int nk0_full, int nk1_full, int g, int S,
+                                                     int &t0, int &nk0, int &nk1) {
+    const int nkv = nk0_full > nk1_full ? nk0_full : nk1_full;
+    const int ta = (int)(((long long)g * nkv) / S), tb = (int)(((long long)(g + 1) * nkv) / S);
+    t0 = ta;
+    const int e0 = (nk0_full < tb ? nk0_full : tb) - ta, e1 = (nk1_full < tb ? nk1_full : tb) - ta;
+    nk0 = e0 > 0 ? e0 : 0;
+    nk1 = e1 > 0 ? e1 : 0;
+}
+
+// Tiles needed from tile 0 by the two query tiles of block mb (rows
+// [256 mb, 256 mb + 256)) of a sequence of `len` rows.
+__host__ __device__ __forceinline__ void block_tiles(int len, int mb, int causal, int &nk0, int &nk1) {
+    const int row0 = mb * 256;
+    const int tiles = (len + 127) / 128;
+    if (causal) {
+        nk0 = tiles < 2 * mb + 1 ? tiles : 2 * mb + 1;
+        nk1 = (row0 + 128 < len) ? (tiles < 2 * mb + 2 ? tiles : 2 * mb + 2) : 0;
+    } else {
+        nk0 = tiles;
+        nk1 = (row0 + 128 < len) ? tiles : 0;
+    }
+}
 
 __device__ __forceinline__ int snake_item(int round, int cta, int G) {
     return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
-// Decode item `idx`; returns false when the item holds no rows.
+// Decode item `idx`; returns false when the item holds no work.  Items are
+// ordered block-from-the-end (heaviest causal blocks first), then split, then
+// (batch, head) / (sequence, head).
+template <bool SPLIT>
 __device__ __forceinline__ bool decode_item(const TcParams &p, int idx, Item &it) {
-    const int blk_from_end = idx / p.units_bh;
-    const int u = idx % p.units_bh;
+    const int S = SPLIT ? p.num_splits : 1;
+    const int per_blk = p.units_bh * S;
+    const int blk_from_end = idx / per_blk;
+    const int rem = idx % per_blk;
+    it.g = rem / p.units_bh;
+    const int u = rem % p.units_bh;
     it.mb = p.num_mblk - 1 - blk_from_end;
     if (p.varlen) {
         const int s = u / p.heads;
@@ -125,18 +168,18 @@ __device__ __forceinline__ bool decode_item(const TcParams &p, int idx, Item &it
         it.start = 0;
         it.len = p.n;
     }
-    const int row0 = it.mb * 2 * BM;
-    if (row0 >= it.len) return false;
-    const int tiles = (it.len + BN - 1) / BN;
-    if (p.causal) {
-        it.nk0 = min(tiles, 2 * it.mb + 1);
-        it.nk1 = (row0 + BM < it.len) ? min(tiles, 2 * it.mb + 2) : 0;
+    if (it.mb * 2 * BM >= it.len) return false;
+    int nk0_full, nk1_full;
+    block_tiles(it.len, it.mb, p.causal, nk0_full, nk1_full);
+    if (SPLIT) {
+        split_range(nk0_full, nk1_full, it.g, S, it.t0, it.nk0, it.nk1);
     } else {
-        it.nk0 = tiles;
-        it.nk1 = (row0 + BM < it.len) ? tiles : 0;
+        it.t0 = 0;
+        it.nk0 = nk0_full;
+        it.nk1 = nk1_full;
     }
     it.nkv = max(it.nk0, it.nk1);
-    return true;
+    return it.nkv > 0;
 }
 
 // Bounded wait by every lane of a warp, with a warp-uniform result (a lane
@@ -198,7 +241,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint6
 }
 
 // --------------------------------------------------------------- kernel --
-template <int D, bool OUT_F32>
+template <int D, int OUT>
 // 10 warps put 3 warps on two of the four SM sub-partitions, whose register
 // files hold 16K registers each: at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -270,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int idx = snake_item(k, cta, G);
                 if (idx >= p.num_items) continue;
                 Item it;
-                if (!decode_item(p, idx, it)) continue;
+                if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
                 if (items > 0 && !mbar_wait(bar_q_empty, (items - 1) & 1, wc, 1)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar_q_full, 2 * C::kTileBytes);
                 for (int s = 0; s < 2; ++s) {
@@ -297,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int hf = 0; hf < C::kHalves; ++hf) {
                             const uint32_t dst = ring + slot * C::kTileBytes + hf * C::kHalfBytes;
                             if (p.varlen)
-                                tma_load_3d(dst, tm, fb, hf * 64, it.h, (int)(it.start + j * BN));
+                                tma_load_3d(dst, tm, fb, hf * 64, it.h, (int)(it.start + (it.t0 + j) * BN));
                             else
-                                tma_load_3d(dst, tm, fb, hf * 64, j * BN, it.bh);
+                                tma_load_3d(dst, tm, fb, hf * 64, (it.t0 + j) * BN, it.bh);
                         }
                         ++lc;
                     }
@@ -329,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item(p, idx, it)) continue;
+            if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
             if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
             ++items;
             tc_fence_after();
@@ -437,10 +480,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item(p, idx, it)) continue;
+            if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
             const int nks = s == 0 ? it.nk0 : it.nk1;
             if (nks == 0) continue;
             const int row = it.mb * 2 * BM + s * BM + r;   // row within the sequence
+            const int len = it.len;
+            const int key_base = it.t0 * BN;               // first key of this split
+            const bool store = row < len;
+            int64_t orow, li;                              // where O and L of this row go
+            if (OUT == kOutPart) {  // dense only: [split][b*h][row]
+                li = ((int64_t)it.g * p.units_bh + it.bh) * p.n + row;
+                orow = li * D;
+            } else if (p.varlen) {
+                orow = ((it.start + row) * p.heads + it.h) * (int64_t)D;
+                li = (int64_t)it.h * p.total + it.start + row;
+            } else {
+                orow = ((int64_t)it.bh * p.n + row) * D;
+                li = (int64_t)it.bh * p.n + row;
+            }
             float m_use = -INFINITY, l = 0.f;
             for (int j = 0; j < nks; ++j) {
                 if (!warp_wait(bar_s_full + 8 * s, sc & 1, wc, 16 + s)) { ok = false; break; }
@@ -451,10 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < BN / 32; ++cc)
                     tmem_ld32(t_s + cc * 32, x + cc * 32);
                 tmem_wait_ld();
-                const int key0 = j * BN;
-                const bool need_mask = (key0 + BN > it.len) || (p.causal && key0 + BN - 1 > row - r);
+                const int key0 = key_base + j * BN;
+                const bool need_mask = (key0 + BN > len) || (p.causal && key0 + BN - 1 > row - r);
                 if (need_mask) {
-                    const int lim = p.causal ? min(row + 1, it.len) : it.len;  // keys < lim are live
+                    const int lim = p.causal ? min(row + 1, len) : len;  // keys < lim are live
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
                         if (key0 + i >= lim) x[i] = -INFINITY;
@@ -524,20 +581,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool live = l > 0.f;
             const float inv = live ? 1.f / l : 0.f;
-            const bool store = row < it.len;
-            int64_t orow;
-            if (p.varlen)
-                orow = ((it.start + row) * p.heads + it.h) * (int64_t)D;
-            else
-                orow = ((int64_t)it.bh * p.n + row) * D;
+            float *const o32 = OUT == kOutPart ? p.ws_o : static_cast<float *>(p.o);
+            float *const lout = OUT == kOutPart ? p.ws_l : p.lse;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float o[32];
                 tmem_ld32(t_o + cc * 32, o);
                 tmem_wait_ld();
                 if (store) {
-                    if (OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + orow + cc * 32);
+                    if (OUT != kOutBf16) {
+                        float4 *dst = reinterpret_cast<float4 *>(o32 + orow + cc * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
@@ -555,11 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            if (store) {
-                const int64_t li = p.varlen ? (int64_t)it.h * p.total + it.start + row
-                                            : (int64_t)it.bh * p.n + row;
-                p.lse[li] = live ? m_use * p.scale + logf(l) : -INFINITY;
-            }
+            if (store) lout[li] = live ? m_use * p.scale + logf(l) : -INFINITY;
         }
     }
 
@@ -621,8 +670,71 @@ int num_sms() {
     return sms;
 }
 
+// Workspace layout of split-key mode: partial O (fp32) then partial L.
+constexpr size_t kWsAlign = 256;
+inline size_t ws_o_bytes(int S, int units, int n, int D) {
+    return ((size_t)S * units * n * D * sizeof(float) + kWsAlign - 1) / kWsAlign * kWsAlign;
+}
+inline size_t ws_l_bytes(int S, int units, int n) {
+    return ((size_t)S * units * n * sizeof(float) + kWsAlign - 1) / kWsAlign * kWsAlign;
+}
+
+// Merge of split-key partials: for each row, L = ln sum_g exp(L_g) and
+// O = sum_g exp(L_g - L) O_g over the splits whose key range holds keys of
+// the row -- the online-softmax rescale of "FlashAttention -- for
+// programmers, not researchers.", STAGE 3, applied across splits.  D/4
+// threads per row, one float4 of O each; HBM-bound.
 template <int D, bool OUT_F32>
-fa_status launch(const FaProblem &pr) {
+__global__ void __launch_bounds__(256)
+    fa_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_l, void *o, float *lse,
+                    int units, int n, int S, int causal) {
+    constexpr int TPR = D / 4;
+    constexpr int RPB = 256 / TPR;
+    const int c4 = threadIdx.x % TPR;
+    const int64_t rows = (int64_t)units * n;
+    for (int64_t r = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; r < rows; r += (int64_t)gridDim.x * RPB) {
+        const int u = (int)(r / n), i = (int)(r % n);
+        const int mb = i / 256, st = (i % 256) / 128;
+        int nk0f, nk1f;
+        block_tiles(n, mb, causal, nk0f, nk1f);
+        float m = -INFINITY;
+        for (int g = 0; g < S; ++g) {
+            int t0, a0, a1;
+            split_range(nk0f, nk1f, g, S, t0, a0, a1);
+            if ((st ? a1 : a0) > 0) m = fmaxf(m, ws_l[((int64_t)g * units + u) * n + i]);
+        }
+        float sum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m != -INFINITY) {
+            for (int g = 0; g < S; ++g) {
+                int t0, a0, a1;
+                split_range(nk0f, nk1f, g, S, t0, a0, a1);
+                if ((st ? a1 : a0) == 0) continue;
+                const int64_t row = ((int64_t)g * units + u) * n + i;
+                const float w = expf(ws_l[row] - m);
+                const float4 og = reinterpret_cast<const float4 *>(ws_o + row * D)[c4];
+                sum += w;
+                acc.x = fmaf(w, og.x, acc.x);
+                acc.y = fmaf(w, og.y, acc.y);
+                acc.z = fmaf(w, og.z, acc.z);
+                acc.w = fmaf(w, og.w, acc.w);
+            }
+        }
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        const int64_t orow = ((int64_t)u * n + i) * D;
+        if (OUT_F32) {
+            reinterpret_cast<float4 *>(static_cast<float *>(o) + orow)[c4] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(o) + orow)[c4] =
+                make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+        }
+        if (c4 == 0) lse[(int64_t)u * n + i] = sum > 0.f ? m + logf(sum) : -INFINITY;
+    }
+}
+
+template <int D, int OUT>
+fa_status launch(const FaProblem &pr, int splits) {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const uint64_t es = 2;
@@ -649,18 +761,26 @@ fa_status launch(const FaProblem &pr) {
     p.n = pr.n;
     p.total = pr.total;
     p.num_mblk = (pr.n + 2 * BM - 1) / (2 * BM);
-    const int64_t items = (int64_t)p.num_mblk * pr.units_bh;
+    p.num_splits = splits;
+    const int64_t items = (int64_t)p.num_mblk * splits * pr.units_bh;
     if (items > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
     p.num_items = (int)items;
+    p.ws_o = nullptr;
+    p.ws_l = nullptr;
+    if (OUT == kOutPart) {
+        uint8_t *ws = static_cast<uint8_t *>(pr.workspace);
+        p.ws_o = reinterpret_cast<float *>(ws);
+        p.ws_l = reinterpret_cast<float *>(ws + ws_o_bytes(splits, pr.units_bh, pr.n, D));
+    }
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.causal = pr.causal;
     p.err = pr.err;
     p.wait_limit_ns = pr.wait_limit_ns;
     int grid = pr.grid_ctas > 0 ? pr.grid_ctas : num_sms();
-    if (grid <= 0) return FA_ERR_CUDA;
+    if (grid <= 0) return FA_ERR_CUDA;  // device query failed (recorded)
     if (grid > p.num_items) grid = p.num_items;
-    auto kern = fa_tc_kernel<D, OUT_F32>;
+    auto kern = fa_tc_kernel<D, OUT>;
     cudaFuncAttributes fattr;
     cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return fa_cuda_fail(e);
@@ -672,13 +792,56 @@ fa_status launch(const FaProblem &pr) {
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
+template <int D, bool OUT_F32>
+fa_status launch_merge(const FaProblem &pr, int splits) {
+    const uint8_t *ws = static_cast<const uint8_t *>(pr.workspace);
+    const float *wo = reinterpret_cast<const float *>(ws);
+    const float *wl = reinterpret_cast<const float *>(ws + ws_o_bytes(splits, pr.units_bh, pr.n, D));
+    constexpr int RPB = 256 / (D / 4);
+    const int64_t rows = (int64_t)pr.units_bh * pr.n;
+    int64_t blocks = (rows + RPB - 1) / RPB;
+    const int cap = (num_sms() > 0 ? num_sms() : 1) * 16;
+    if (blocks > cap) blocks = cap;
+    fa_merge_kernel<D, OUT_F32><<<(int)blocks, 256, 0, pr.stream>>>(wo, wl, pr.o, pr.lse, pr.units_bh, pr.n,
+                                                                     splits, pr.causal);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
+}
+
+template <int D>
+fa_status launch_d(const FaProblem &pr) {
+    const bool f32 = pr.dtype == FA_BF16_OUT_F32;
+    if (pr.num_splits <= 1) return f32 ? launch<D, kOutF32>(pr, 1) : launch<D, kOutBf16>(pr, 1);
+    const fa_status st = launch<D, kOutPart>(pr, pr.num_splits);
+    if (st != FA_OK) return st;
+    return f32 ? launch_merge<D, true>(pr, pr.num_splits) : launch_merge<D, false>(pr, pr.num_splits);
+}
+
 }  // namespace
 }  // namespace fa
 
+bool fa_tc_split_plan(int units_bh, int n, int D, int requested, int &splits, size_t &bytes) {
+    const int num_mblk = (n + 2 * fa::BM - 1) / (2 * fa::BM);
+    const int tiles = (n + fa::BN - 1) / fa::BN;
+    int S = requested;
+    if (S <= 0) {
+        const int sms = fa::num_sms();
+        if (sms <= 0) return false;
+        const int64_t items = (int64_t)num_mblk * units_bh;
+        S = items >= sms ? 1 : (int)((sms + items - 1) / items);
+    }
+    if (S > tiles) S = tiles;
+    if (S > 64) S = 64;
+    if (S < 1) S = 1;
+    splits = S;
+    bytes = S > 1 ? fa::ws_o_bytes(S, units_bh, n, D) + fa::ws_l_bytes(S, units_bh, n) : 0;
+    return true;
+}
+
 fa_status fa_launch_tc(const FaProblem &pr) {
     if (pr.dtype != FA_BF16 && pr.dtype != FA_BF16_OUT_F32) return FA_ERR_UNSUPPORTED;
-    const bool f32 = pr.dtype == FA_BF16_OUT_F32;
-    if (pr.D == 64) return f32 ? fa::launch<64, true>(pr) : fa::launch<64, false>(pr);
-    if (pr.D == 128) return f32 ? fa::launch<128, true>(pr) : fa::launch<128, false>(pr);
+    if (pr.num_splits > 1 && pr.varlen) return FA_ERR_UNSUPPORTED;
+    if (pr.D == 64) return fa::launch_d<64>(pr);
+    if (pr.D == 128) return fa::launch_d<128>(pr);
     return FA_ERR_UNSUPPORTED;
 }

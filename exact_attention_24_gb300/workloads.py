@@ -120,4 +120,8 @@ C4 = Workload("B1_H32_N8192_D64_bf16_causal_qk2", 1, 32, 8192, 64, "bf16",
 C5 = Workload("varlen16_H16_D128_bf16_causal", 0, 16, 0, 128, "bf16", True,
               4, lengths=varlen_lengths(16, 128, 4096, 4))
 
-WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C5)}
+# Few (batch, head) units and a long sequence: 64 causal 256-row blocks per
+# head x 2 heads = 128 work items for 152 SMs, the case split keys are for.
+SPLIT_LONG = Workload("B1_H2_N16384_D128_bf16_causal", 1, 2, 16384, 128, "bf16", True, 5)
+
+WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C5, SPLIT_LONG)}

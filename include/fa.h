@@ -43,6 +43,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -123,6 +124,44 @@ FA_API fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void
                         int total_tokens, int max_seqlen, int H, int D,
                         float scale, int causal, fa_dtype dtype,
                         fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv -- dense batch with each 256-row query block's keys cut into
+ * `num_splits` contiguous ranges processed by separate work items, for
+ * problems with too few (batch, head, query-block) units to fill the GPU
+ * (small B*H, long N).  Each range produces a partial result normalised over
+ * its own keys (O_g in fp32, L_g) in `workspace`; a merge kernel then
+ * computes L = ln sum_g exp(L_g) and O = sum_g exp(L_g - L) O_g, which is the
+ * online-softmax rescale of "FlashAttention -- for programmers, not
+ * researchers.", STAGE 3, applied across ranges.  Same result as fa_fwd up
+ * to rounding.
+ *
+ *   Q, K, V, O, L, B, H, N, D, scale, causal : as fa_fwd
+ *   dtype           : FA_BF16 or FA_BF16_OUT_F32 (FA_F32: FA_ERR_UNSUPPORTED)
+ *   num_splits      : 1..64, or 0 to choose automatically (enough work items
+ *                     to cover the SMs); capped at ceil(N / 128)
+ *   workspace       : caller-owned DEVICE memory, 16-byte aligned, at least
+ *                     fa_fwd_splitkv_workspace_size(...) bytes; its contents
+ *                     on entry do not matter and are garbage on exit.  May be
+ *                     NULL when that size is 0 (a single split).
+ *   workspace_bytes : its size
+ *
+ * Two kernels are enqueued on `stream`; calls that share a workspace must be
+ * ordered on the GPU.
+ */
+FA_API fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O,
+                                float *L, int B, int H, int N, int D, float scale,
+                                int causal, fa_dtype dtype, int num_splits,
+                                void *workspace, size_t workspace_bytes,
+                                fa_stream_t stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for these sizes and `num_splits`
+ * (0 = the automatic choice, made for the current device).  Returns 0 when a
+ * single split is used (or on an invalid size or a failed device query).
+ */
+FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int D,
+                                            int num_splits);
 
 /*
  * fa_check_device_error -- synchronise `stream`, then return (and clear)

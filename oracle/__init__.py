@@ -14,6 +14,8 @@ The oracle is written from the definition of attention, in float64 NumPy:
   output of "Kernel visualization: Flash Attention 2", sections
   "Iteration j = 0" (scale after the dot product) and "Write the data back
   to HBM" (the L array).
+* ``merge_partials`` -- STAGE 3's running-max / running-sum rescale applied
+  to results computed over disjoint key ranges (the split-key merge).
 * ``attention_tiled`` -- the tiled online-softmax loop of the same script's
   STAGE 3 (online softmax) and STAGE 4 (FlashAttention), used to pin the
   one-pass definition (block-size invariance) and to show that the
@@ -28,4 +30,5 @@ from .attention import (  # noqa: F401
     attention_ref_varlen,
     attention_tiled,
     attention_rows,
+    merge_partials,
 )

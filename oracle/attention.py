@@ -49,22 +49,28 @@ def _f64(x) -> np.ndarray:
 
 
 def _attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-            causal: bool, row_pos: np.ndarray):
+            causal: bool, row_pos: np.ndarray, key_lo: int = 0, key_hi=None):
     """One head of standard attention for the query rows ``q`` whose
-    positions in the sequence are ``row_pos``.
+    positions in the sequence are ``row_pos``, over the keys at positions
+    ``key_lo <= j < key_hi`` only (all keys by default; the causal mask uses
+    absolute positions).
 
     q: [r, d]; k, v: [n, d]; returns (O [r, d], L [r]) in float64.
     """
     r, d = q.shape
     n = k.shape[0]
+    key_hi = n if key_hi is None else min(int(key_hi), n)
+    key_lo = max(0, int(key_lo))
     o = np.zeros((r, v.shape[1]), dtype=np.float64)
     lse = np.full(r, -np.inf, dtype=np.float64)
     if r == 0 or n == 0:
         return o, lse
     # STAGE 2: the full score block, scaled after the dot product.
     s = scale * (q @ k.T)
+    key_pos = np.arange(n)
+    outside = (key_pos < key_lo) | (key_pos >= key_hi)
+    s = np.where(outside[None, :], -np.inf, s)
     if causal:
-        key_pos = np.arange(n)
         s = np.where(key_pos[None, :] > row_pos[:, None], -np.inf, s)
     # STAGE 1: subtract the row max, exponentiate, normalise.
     m = s.max(axis=1)
@@ -97,15 +103,51 @@ def attention_ref(q, k, v, scale: float, causal: bool):
     return o.reshape(*lead, n, vf.shape[-1]), lse.reshape(*lead, n)
 
 
-def attention_rows(q, k, v, scale: float, causal: bool, rows):
-    """Standard attention for selected query rows of ONE head.
+def attention_rows(q, k, v, scale: float, causal: bool, rows, key_lo: int = 0,
+                   key_hi=None):
+    """Standard attention for selected query rows of ONE head, optionally
+    over a sub-range of the keys ``[key_lo, key_hi)`` (positions absolute).
 
     q, k, v: ``[N, D]``; ``rows``: integer positions.  Used to check outputs
-    of workloads too large for the full oracle, one row at a time.
+    of workloads too large for the full oracle, one row at a time, and the
+    partial results of a split key range.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     rows = np.asarray(rows, dtype=np.int64)
-    return _attend(q[rows], k, v, float(scale), causal, rows)
+    return _attend(q[rows], k, v, float(scale), causal, rows, key_lo, key_hi)
+
+
+def merge_partials(o_parts, l_parts):
+    """Combine attention results computed over disjoint key ranges.
+
+    o_parts: ``[G, ..., D]`` -- each part normalised over its own keys;
+    l_parts: ``[G, ...]`` -- each part's log-sum-exp (``-inf`` for a part with
+    no key).  This is STAGE 3's online-softmax update applied part by part:
+    carry a running max ``m`` and running sum ``l`` of exp(score - m) plus the
+    unnormalised output; when a part raises the max, rescale what was carried
+    by exp(m_old - m_new); normalise once at the end.  Returns ``(O, L)``.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    l_parts = np.asarray(l_parts, dtype=np.float64)
+    m = np.full(l_parts.shape[1:], -np.inf)
+    l = np.zeros(l_parts.shape[1:])
+    acc = np.zeros(o_parts.shape[1:])
+    for g in range(l_parts.shape[0]):
+        lg = l_parts[g]
+        m_new = np.maximum(m, lg)
+        live = np.isfinite(m_new)
+        m_use = np.where(live, m_new, 0.0)
+        carry = np.where(np.isfinite(m), np.exp(m - m_use), 0.0)   # rescale of the carry
+        w = np.where(np.isfinite(lg), np.exp(lg - m_use), 0.0)     # this part's sum, on m_use
+        l = carry * l + w
+        acc = carry[..., None] * acc + w[..., None] * o_parts[g]
+        m = m_new
+    live = l > 0
+    o = np.zeros_like(acc)
+    o[live] = acc[live] / l[live, None]
+    lse = np.full(l.shape, -np.inf)
+    lse[live] = m[live] + np.log(l[live])
+    return o, lse
 
 
 def attention_ref_varlen(q, k, v, cu_seqlens, scale: float, causal: bool):

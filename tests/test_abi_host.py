@@ -143,3 +143,30 @@ def test_product_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not pat.search(text), f
+
+
+def test_splitkv_argument_checks(lib):
+    q, k, v, o, l = _ptrs()
+    ws = A + 6 * STEP
+    bad = fa.FA_ERR_INVALID_ARG
+    args = (q, k, v, o, l, 1, 1, 1024, 128, 0.1, 1)
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, 65, ws, 1 << 30, 0) == bad
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, -1, ws, 1 << 30, 0) == bad
+    assert fa.fa_fwd_splitkv(*args, fa.FA_F32, 3, ws, 1 << 30, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, 3, 0, 1 << 30, 0) == bad        # no workspace
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, 3, ws + 8, 1 << 30, 0) == bad   # misaligned
+    need = fa.fa_fwd_splitkv_workspace_size(1, 1, 1024, 128, 3)
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, 3, ws, need - 1, 0) == bad      # too small
+    assert fa.fa_fwd_splitkv(*args, fa.FA_BF16, 3, q, need, 0) == bad           # overlaps Q
+
+
+def test_splitkv_workspace_size(lib):
+    # partial O in fp32 then partial L, each padded to 256 bytes
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1024, 128, 3) == 3 * 1024 * 128 * 4 + 3 * 1024 * 4
+    assert fa.fa_fwd_splitkv_workspace_size(2, 3, 1000, 64, 4) == \
+        -(-4 * 6 * 1000 * 64 * 4 // 256) * 256 + -(-4 * 6 * 1000 * 4 // 256) * 256
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1024, 128, 1) == 0     # one split: none needed
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 9) == \
+        fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 3)                # capped at ceil(N/128)
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1024, 96, 3) == 0      # unsupported D
+    assert fa.fa_fwd_splitkv_workspace_size(0, 1, 1024, 128, 3) == 0

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 from oracle import (attention_ref, attention_ref_varlen, attention_rows,
-                    attention_tiled)
+                    attention_tiled, merge_partials)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -330,3 +330,77 @@ def test_bf16_inputs_are_upcast_exactly():
     O2, L2 = attention_ref(x.double().numpy(), x.double().numpy(),
                            x.double().numpy(), 0.5, False)
     assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
+# ---------------------------------------------------------------------------
+# key ranges and the split-key merge
+# ---------------------------------------------------------------------------
+def _split_points(n, g, rng):
+    cuts = np.sort(rng.choice(np.arange(1, n), size=g - 1, replace=False)) if g > 1 else []
+    return [0, *[int(c) for c in cuts], n]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("parts", [1, 2, 3, 7])
+def test_merge_of_key_ranges_is_full_attention(causal, parts):
+    """Attention over disjoint key ranges, merged, is attention over all keys
+    (the identity behind split-key attention), to float64 noise."""
+    r = _rng(20 + parts)
+    n, d = 61, 8
+    q, k, v = r.normal(size=(n, d)) * 2, r.normal(size=(n, d)) * 2, r.normal(size=(n, 5))
+    rows = np.arange(n)
+    cuts = _split_points(n, parts, r)
+    O_p, L_p = zip(*[attention_rows(q, k, v, 0.4, causal, rows, a, b)
+                     for a, b in zip(cuts[:-1], cuts[1:])])
+    O, L = merge_partials(np.stack(O_p), np.stack(L_p))
+    Of, Lf = attention_ref(q, k, v, 0.4, causal)
+    assert np.max(np.abs(O - Of)) <= 1e-13 and np.max(np.abs(L - Lf)) <= 1e-12
+    # part order does not matter
+    perm = r.permutation(len(O_p))
+    O2, L2 = merge_partials(np.stack(O_p)[perm], np.stack(L_p)[perm])
+    assert np.max(np.abs(O2 - Of)) <= 1e-13 and np.max(np.abs(L2 - Lf)) <= 1e-12
+
+
+def test_key_range_brute_force():
+    """A key sub-range is plain attention over those keys (brute force)."""
+    r = _rng(30)
+    n, d = 7, 3
+    q, k, v = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, 2))
+    for causal in (False, True):
+        for a, b in [(0, 7), (2, 5), (3, 4), (5, 7)]:
+            O, L = attention_rows(q, k, v, 0.8, causal, np.arange(n), a, b)
+            for i in range(n):
+                keys = [j for j in range(a, b) if not (causal and j > i)]
+                if not keys:
+                    assert L[i] == -np.inf and np.all(O[i] == 0)
+                    continue
+                w = [math.exp(0.8 * math.fsum(q[i][t] * k[j][t] for t in range(d))) for j in keys]
+                z = math.fsum(w)
+                assert abs(L[i] - math.log(z)) <= 1e-14
+                for c in range(2):
+                    ref = math.fsum(w[x] * v[j][c] for x, j in enumerate(keys)) / z
+                    assert abs(O[i][c] - ref) <= 1e-14
+
+
+def test_merge_special_cases():
+    r = _rng(31)
+    o = r.normal(size=(4, 6, 3))
+    l = r.normal(size=(4, 6))
+    # one part: identity
+    O, L = merge_partials(o[:1], l[:1])
+    assert np.allclose(O, o[0], atol=1e-15) and np.allclose(L, l[0], atol=1e-15)
+    # empty parts (L = -inf) are ignored
+    l2 = l.copy()
+    l2[1] = -np.inf
+    O, L = merge_partials(o, l2)
+    O3, L3 = merge_partials(o[[0, 2, 3]], l[[0, 2, 3]])
+    assert np.allclose(O, O3, atol=1e-14) and np.allclose(L, L3, atol=1e-14)
+    # all parts empty: O = 0, L = -inf
+    O, L = merge_partials(o, np.full_like(l, -np.inf))
+    assert np.all(O == 0) and np.all(L == -np.inf)
+    # two equal parts: O unchanged, L + ln 2
+    O, L = merge_partials(np.stack([o[0], o[0]]), np.stack([l[0], l[0]]))
+    assert np.allclose(O, o[0], atol=1e-14) and np.allclose(L, l[0] + math.log(2), atol=1e-14)
+    # huge L values do not overflow
+    O, L = merge_partials(np.stack([o[0], o[1]]), np.stack([l[0] + 800, l[1] + 810]))
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))

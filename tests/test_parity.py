@@ -280,3 +280,56 @@ def test_watchdog_timeout_reports_and_recovers():
     O, L = run_dense(q.to(DEV), k.to(DEV), v.to(DEV), True, fa.FA_BF16_OUT_F32, w.scale)
     ref_o, ref_l = attention_ref(q, k, v, w.scale, True)
     assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_BF16_OUT_F32, "after watchdog")
+
+
+# ------------------------------------------------------------ split keys --
+def run_splitkv(q, k, v, causal, code, scale, splits):
+    B, H, N, D = q.shape
+    O = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16 if code == fa.FA_BF16 else torch.float32,
+                   device=q.device)
+    L = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
+    nbytes = fa.fa_fwd_splitkv_workspace_size(B, H, N, D, splits)
+    ws = torch.full((max(nbytes, 16) // 4,), float("nan"), dtype=torch.float32, device=q.device)
+    st = fa.fa_fwd_splitkv(q, k, v, O, L, B, H, N, D, scale, int(causal), code, splits, ws, nbytes, None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    return O, L
+
+
+@pytest.mark.parametrize("case", [(1, 1, 4096, 128, True, 8), (1, 2, 3000, 64, False, 3),
+                                  (2, 1, 1000, 128, True, 0), (1, 1, 300, 64, True, 5),
+                                  (1, 3, 777, 128, False, 2), (1, 1, 2048, 64, True, 16)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_splitkv_matches_oracle(case):
+    B, H, N, D, causal, splits = case
+    w, q, k, v = _dense_case(B, H, N, D, "bf16", causal, seed=N + splits)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, causal)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for code in BF16_CODES:
+        O, L = run_splitkv(qd, kd, vd, causal, code, w.scale, splits)
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"split {case} dt={code}")
+
+
+def test_splitkv_one_split_is_the_dense_path():
+    w, q, k, v = _dense_case(1, 2, 1500, 128, "bf16", True, seed=9)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    O1, L1 = run_splitkv(qd, kd, vd, True, fa.FA_BF16, w.scale, 1)
+    O2, L2 = run_dense(qd, kd, vd, True, fa.FA_BF16, w.scale)
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+def test_splitkv_merge_agrees_with_oracle_merge():
+    """The GPU merge of the GPU's own partials against the oracle's merge of
+    the oracle's partials over the same key ranges (C4-like sharp softmax)."""
+    from oracle import merge_partials
+    w, q, k, v = _dense_case(1, 1, 2048, 64, "bf16", True, seed=4, qk_mult=2.0)
+    O, L = run_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), True, fa.FA_BF16_OUT_F32, w.scale, 4)
+    rows = sample_rows(2048, 64, seed=3)
+    ref_o, ref_l = attention_rows(q[0, 0], k[0, 0], v[0, 0], w.scale, True, rows)
+    assert_close(to_f64(O[0, 0, rows]), to_f64(L[0, 0, rows]), ref_o, ref_l, fa.FA_BF16_OUT_F32, "merge")
+    # the oracle's own split-and-merge over 128-key-aligned ranges agrees too
+    cuts = [0, 512, 1024, 1536, 2048]
+    parts = [attention_rows(q[0, 0], k[0, 0], v[0, 0], w.scale, True, rows, a, b)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    mo, ml = merge_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    assert np.max(np.abs(mo - ref_o)) < 1e-12 and np.max(np.abs(ml - ref_l)) < 1e-12
