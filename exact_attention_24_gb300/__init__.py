@@ -27,7 +27,7 @@ __all__ = [
     "FA_ERR_DEVICE_TIMEOUT", "FA_F32", "FA_BF16", "FA_BF16_OUT_F32",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_TC", "FaError",
     "load_library", "library_path", "fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
-    "fa_fwd_splitkv_workspace_size",
+    "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
     "attention_varlen", "EXPORTED_SYMBOLS",
@@ -39,7 +39,8 @@ FA_F32, FA_BF16, FA_BF16_OUT_F32 = 0, 1, 2
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
-                    "fa_fwd_splitkv_workspace_size", "fa_check_device_error",
+                    "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc",
+                    "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
                     "fa_get_options", "fa_watchdog_selftest")
 
@@ -91,6 +92,9 @@ def load_library():
     lib.fa_fwd_splitkv.restype = i32
     lib.fa_fwd_splitkv_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+    lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                           i32, i32, i32, vp]
+    lib.fa_fwd_splitkv_noalloc.restype = i32
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -152,6 +156,19 @@ def fa_fwd_splitkv(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, num_splits,
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), int(B), int(H), int(N), int(D),
         float(scale), int(causal), int(dtype), int(num_splits), _ptr(workspace),
         int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_splitkv_noalloc(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, num_splits,
+                           stream=None) -> int:
+    """Split-key forward pass that allocates nothing: for callers that may
+    not allocate device memory (see include/fa.h).  Partials go to the
+    library's fixed scratch array (FA_NOALLOC_SCRATCH_BYTES)."""
+    return load_library().fa_fwd_splitkv_noalloc(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), int(B), int(H), int(N), int(D),
+        float(scale), int(causal), int(dtype), int(num_splits), _stream(stream))
+
+
+FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 def fa_fwd_splitkv_workspace_size(B, H, N, D, num_splits) -> int:

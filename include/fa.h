@@ -164,6 +164,36 @@ FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int D,
                                             int num_splits);
 
 /*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory: a plugin inside a host program that owns the device-memory
+ * budget, a latency-critical caller that must not call cudaMalloc/cudaFree
+ * (they can synchronise the device), or C code handed only its inputs and
+ * outputs.  The pages have no counterpart of this entry point: it changes
+ * where the split-key partials live, not what is computed.
+ *
+ * Arguments and results are those of fa_fwd_splitkv, without the workspace.
+ * The partials go to one scratch array of FA_NOALLOC_SCRATCH_BYTES bytes in
+ * the library, which every GPU that loads the library holds until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ *  - Sizes whose split workspace (fa_fwd_splitkv_workspace_size) exceeds
+ *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED before
+ *    anything is enqueued.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query, no allocation) with that device current; make that first
+ *    call before any stream capture on the device.
+ *  - All calls share the array: calls that overlap on the GPU (other
+ *    streams, other host threads) race on it.  Order them on one stream.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+FA_API fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V,
+                                        void *O, float *L, int B, int H, int N, int D,
+                                        float scale, int causal, fa_dtype dtype,
+                                        int num_splits, fa_stream_t stream);
+
+/*
  * fa_check_device_error -- synchronise `stream`, then return (and clear)
  * the status recorded by kernels of this library on the current device:
  * FA_ERR_DEVICE_TIMEOUT if a device wait ran out, FA_ERR_INVALID_ARG if a
