@@ -58,6 +58,11 @@ constexpr int kOutBf16 = 0;   // O bf16, L
 constexpr int kOutF32 = 1;    // O fp32, L
 constexpr int kOutPart = 2;   // split-key partial: O_g fp32 and L_g into the workspace
 
+// Varlen batches with at most kMaxSchedSeqs sequences and kMaxSchedLevels
+// 256-row blocks per sequence get a compact schedule (see decode_item).
+constexpr int kMaxSchedSeqs = 384;
+constexpr int kMaxSchedLevels = 128;
+
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 64;                    // 128-byte swizzle atoms per row
@@ -68,7 +73,9 @@ struct Cfg {
     static constexpr int kRingOff = kQBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+    static constexpr int kSchedOff = kBarOff + kBarBytes;         // varlen schedule table
+    static constexpr int kSchedBytes = 2 * (kMaxSchedSeqs + kMaxSchedLevels);
+    static constexpr int kSmemBytes = kSchedOff + kSchedBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(kBarBytes >= 8 * (2 + 2 * kSlots + 6) + 16, "barrier area");
 };
@@ -84,6 +91,8 @@ struct TcParams {
     int64_t total;    // varlen: total tokens
     int num_mblk;     // ceil(n / 256)
     int num_splits;   // key-range splits per block (1 = none)
+    int num_seqs;     // varlen: sequences
+    int compact;      // varlen: use the compact schedule table
     int num_items;    // num_mblk * num_splits * units_bh
     float *ws_o;      // split mode: partial O, fp32 [splits][units][n][D]
     float *ws_l;      // split mode: partial L, fp32 [splits][units][n]
@@ -144,8 +153,50 @@ __device__ __forceinline__ int snake_item(int round, int cta, int G) {
 // Decode item `idx`; returns false when the item holds no work.  Items are
 // ordered block-from-the-end (heaviest causal blocks first), then split, then
 // (batch, head) / (sequence, head).
+// Shared-memory schedule of a varlen batch: the sequences ranked by their
+// number of 256-row blocks (longest first, ties by index) and, per block
+// level L, how many sequences reach it.  Built once per CTA; every role
+// decodes from it, so all agree on the order.
+struct Sched {
+    const uint16_t *ranked;   // [num_seqs] sequence ids, longest first
+    const uint16_t *reach;    // [num_mblk] #sequences with more than L blocks
+};
+
+// Varlen compact order: level L from the top, then the sequences that reach
+// L (longest first), then heads -- only items that hold work, so the snake
+// assignment spreads real work evenly instead of walking empty slots.
+__device__ __forceinline__ bool decode_varlen_compact(const TcParams &p, const Sched &sc, int idx,
+                                                      Item &it) {
+    int L = p.num_mblk - 1;
+    for (; L >= 0; --L) {
+        const int here = (int)sc.reach[L] * p.heads;
+        if (idx < here) break;
+        idx -= here;
+    }
+    if (L < 0) return false;
+    const int seq = sc.ranked[idx / p.heads];
+    it.h = idx % p.heads;
+    it.bh = 0;
+    it.g = 0;
+    it.mb = L;
+    int64_t start;
+    int len;
+    if (!seq_bounds(p.cu, seq, p.total, p.n, p.err, start, len)) return false;
+    it.start = start;
+    it.len = len;
+    if (it.mb * 2 * BM >= it.len) return false;
+    int nk0_full, nk1_full;
+    block_tiles(it.len, it.mb, p.causal, nk0_full, nk1_full);
+    it.t0 = 0;
+    it.nk0 = nk0_full;
+    it.nk1 = nk1_full;
+    it.nkv = max(it.nk0, it.nk1);
+    return it.nkv > 0;
+}
+
 template <bool SPLIT>
-__device__ __forceinline__ bool decode_item(const TcParams &p, int idx, Item &it) {
+__device__ __forceinline__ bool decode_item(const TcParams &p, const Sched &sc, int idx, Item &it) {
+    if (!SPLIT && p.compact) return decode_varlen_compact(p, sc, idx, it);
     const int S = SPLIT ? p.num_splits : 1;
     const int per_blk = p.units_bh * S;
     const int blk_from_end = idx / per_blk;
@@ -294,6 +345,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // Varlen compact schedule: rank the sequences by block count and count
+    // how many reach each block level.  The lengths are staged in the (not
+    // yet used) K/V ring; TMA writes there only after the barrier below.
+    uint16_t *sched_ranked = reinterpret_cast<uint16_t *>(gbase + C::kSchedOff);
+    uint16_t *sched_reach = sched_ranked + kMaxSchedSeqs;
+    if (p.compact) {
+        int *nblk = reinterpret_cast<int *>(gbase + C::kRingOff);
+        for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+            int64_t start;
+            int len;
+            seq_bounds(p.cu, q, p.total, p.n, p.err, start, len);  // invalid: len = 0
+            nblk[q] = (len + 2 * BM - 1) / (2 * BM);
+        }
+        __syncthreads();
+        for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+            const int nq = nblk[q];
+            int rank = 0;
+            for (int t = 0; t < p.num_seqs; ++t) {
+                const int nt = nblk[t];
+                rank += (nt > nq) || (nt == nq && t < q);
+            }
+            sched_ranked[rank] = (uint16_t)q;
+        }
+        for (int L = threadIdx.x; L < p.num_mblk; L += blockDim.x) {
+            int reach = 0;
+            for (int t = 0; t < p.num_seqs; ++t) reach += nblk[t] > L;
+            sched_reach[L] = (uint16_t)reach;
+        }
+        // generic-proxy use of the ring is over before TMA (async proxy) writes it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    const Sched sched{sched_ranked, sched_reach};
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -313,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int idx = snake_item(k, cta, G);
                 if (idx >= p.num_items) continue;
                 Item it;
-                if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
+                if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
                 if (items > 0 && !mbar_wait(bar_q_empty, (items - 1) & 1, wc, 1)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar_q_full, 2 * C::kTileBytes);
                 for (int s = 0; s < 2; ++s) {
@@ -372,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
+            if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
             if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
             ++items;
             tc_fence_after();
@@ -480,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item<OUT == kOutPart>(p, idx, it)) continue;
+            if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
             const int nks = s == 0 ? it.nk0 : it.nk1;
             if (nks == 0) continue;
             const int row = it.mb * 2 * BM + s * BM + r;   // row within the sequence
@@ -762,6 +845,8 @@ fa_status launch(const FaProblem &pr, int splits) {
     p.total = pr.total;
     p.num_mblk = (pr.n + 2 * BM - 1) / (2 * BM);
     p.num_splits = splits;
+    p.num_seqs = pr.num_seqs;
+    p.compact = pr.varlen && pr.num_seqs <= kMaxSchedSeqs && p.num_mblk <= kMaxSchedLevels;
     const int64_t items = (int64_t)p.num_mblk * splits * pr.units_bh;
     if (items > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
     p.num_items = (int)items;
