@@ -72,12 +72,19 @@ struct Cfg {
     static constexpr int kQBytes = 2 * kTileBytes;
     static constexpr int kRingOff = kQBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-    static constexpr int kBarBytes = 256;
+    // D=128 fills TMEM with S_0, S_1, O_0, O_1, so P_s overwrites S_s and the
+    // next Q K^T must follow P V.  At D=64 P_s gets columns of its own: the
+    // next S_s is computed as soon as the softmax has read S_s, so the
+    // softmax warps never wait for S.
+    static constexpr bool kPAlias = (D == 128);
+    static constexpr int kBarBytes = kPAlias ? 256 : 512;
     static constexpr int kSchedOff = kBarOff + kBarBytes;         // varlen schedule table
     static constexpr int kSchedBytes = 2 * (kMaxSchedSeqs + kMaxSchedLevels);
     static constexpr int kSmemBytes = kSchedOff + kSchedBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(kBarBytes >= 8 * (2 + 2 * kSlots + 6) + 16, "barrier area");
+    // q full/empty, ring full/empty, s_full, p_full, o_final, s_free, pv_done
+    // (two each), drain, then the TMEM address and the abort flag.
+    static_assert(kBarBytes >= 8 * (2 + 2 * kSlots + 10 + 1) + 16, "barrier area");
 };
 
 struct TcParams {
@@ -241,6 +248,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
 }
 
+// Wait (whole warp) until ring load number `li` has landed in its slot.
+__device__ __forceinline__ bool ring_wait(uint32_t bar_full, uint32_t li, uint32_t slots, const WaitCtx &w,
+                                          uint32_t site) {
+    return warp_wait(bar_full + 8 * (li % slots), (li / slots) & 1, w, site);
+}
+
 // ------------------------------------------------ UMMA descriptor helpers --
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and
 // stride-dimension byte offsets (>> 4), fixed version bits 46-47 = 1,
@@ -315,7 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_s_full = bar_kv_empty + 8 * C::kSlots;  // [2]
     const uint32_t bar_p_full = bar_s_full + 16;               // [2]
     const uint32_t bar_o_final = bar_p_full + 16;              // [2]
-    const uint32_t bar_drain = bar_o_final + 16;
+    const uint32_t bar_s_free = bar_o_final + 16;              // [2] S_s read (D=64)
+    const uint32_t bar_pv_done = bar_s_free + 16;              // [2] P_s V done (D=64)
+    const uint32_t bar_drain = bar_pv_done + 16;
     uint8_t *gbars = gbase + C::kBarOff;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + C::kBarBytes - 8);
@@ -333,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_s_full + 8 * s, 1);
             mbar_init(bar_p_full + 8 * s, 4);
             mbar_init(bar_o_final + 8 * s, 1);
+            mbar_init(bar_s_free + 8 * s, 4);
+            mbar_init(bar_pv_done + 8 * s, 1);
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -449,9 +466,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint64_t kSlotDesc = C::kTileBytes >> 4;  // one slot in descriptor units
         const uint32_t t_s0 = tmem, t_s1 = tmem + BN;
         const uint32_t t_o0 = tmem + 2 * BN, t_o1 = tmem + 2 * BN + D;
-        uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0;
+        uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0, fc0 = 0, fc1 = 0;
         bool ok = true;
-        for (int k = 0; ok && k * G < p.num_items; ++k) {
+        if (!C::kPAlias) {
+            // D=64: P_s has its own TMEM columns.  Per K/V tile j: both next
+            // Q K^T as soon as the softmaxes have read S(j), then both P V.
+            const uint32_t t_p0 = tmem + 2 * BN + 2 * D, t_p1 = t_p0 + BN / 2;
+            for (int k = 0; ok && k * G < p.num_items; ++k) {
+                const int idx = snake_item(k, cta, G);
+                if (idx >= p.num_items) continue;
+                Item it;
+                if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
+                if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
+                ++items;
+                tc_fence_after();
+                const uint32_t l0 = lc;
+                lc += 2 * it.nkv;
+                if (!ring_wait(bar_kv_full, l0, C::kSlots, wc, 4)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint64_t dk0 = dk_ring + (l0 % C::kSlots) * kSlotDesc;
+                    issue_qk<D>(t_s0, dq0, dk0);
+                    mma_commit(bar_s_full);
+                    if (it.nk1 > 0) {
+                        issue_qk<D>(t_s1, dq1, dk0);
+                        mma_commit(bar_s_full + 8);
+                    }
+                    mma_commit(bar_kv_empty + 8 * (l0 % C::kSlots));
+                    if (it.nkv == 1) mma_commit(bar_q_empty);
+                }
+                __syncwarp();
+                for (int j = 0; j < it.nkv; ++j) {
+                    const uint32_t li_v = l0 + 2 * j + 1, li_kn = li_v + 1;
+                    const bool need0 = j + 1 < it.nk0, need1 = j + 1 < it.nk1;
+                    if (need0 || need1) {
+                        if (!ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8)) { ok = false; break; }
+                        const uint64_t dkn = dk_ring + (li_kn % C::kSlots) * kSlotDesc;
+                        if (need0) {
+                            if (!warp_wait(bar_s_free, fc0 & 1, wc, 10)) { ok = false; break; }
+                            ++fc0;
+                            tc_fence_after();
+                            if (elect_one()) {
+                                issue_qk<D>(t_s0, dq0, dkn);
+                                mma_commit(bar_s_full);
+                            }
+                            __syncwarp();
+                        }
+                        if (need1) {
+                            if (!warp_wait(bar_s_free + 8, fc1 & 1, wc, 11)) { ok = false; break; }
+                            ++fc1;
+                            tc_fence_after();
+                            if (elect_one()) {
+                                issue_qk<D>(t_s1, dq1, dkn);
+                                mma_commit(bar_s_full + 8);
+                            }
+                            __syncwarp();
+                        }
+                        if (elect_one()) {  // K_{j+1} has had its last reader issued
+                            mma_commit(bar_kv_empty + 8 * (li_kn % C::kSlots));
+                            if (j + 1 == it.nkv - 1) mma_commit(bar_q_empty);
+                        }
+                        __syncwarp();
+                    }
+                    if (!ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5)) { ok = false; break; }
+                    const uint64_t dv = dv_ring + (li_v % C::kSlots) * kSlotDesc;
+                    if (j < it.nk0) {
+                        if (!warp_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
+                        ++pc0;
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_pv<D>(t_o0, t_p0, dv, j > 0 ? 1u : 0u);
+                            mma_commit(bar_pv_done);
+                        }
+                        __syncwarp();
+                    }
+                    if (j < it.nk1) {
+                        if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
+                        ++pc1;
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_pv<D>(t_o1, t_p1, dv, j > 0 ? 1u : 0u);
+                            mma_commit(bar_pv_done + 8);
+                        }
+                        __syncwarp();
+                    }
+                    if (elect_one()) mma_commit(bar_kv_empty + 8 * (li_v % C::kSlots));
+                    __syncwarp();
+                }
+            }
+        }
+        for (int k = 0; C::kPAlias && ok && k * G < p.num_items; ++k) {
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
@@ -554,10 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;     // TMEM lane quarter
         const int r = quarter * 32 + lane;  // row within the query tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t t_s = tmem + lane_off + s * BN;           // S_s / P_s
+        const uint32_t t_s = tmem + lane_off + s * BN;           // S_s
         const uint32_t t_o = tmem + lane_off + 2 * BN + s * D;   // O_s
+        const uint32_t t_p = C::kPAlias ? t_s : tmem + lane_off + 2 * BN + 2 * D + s * (BN / 2);  // P_s
         const float c = p.scale_log2;
-        uint32_t sc = 0, oc = 0;  // S_full and O_final phases consumed
+        uint32_t sc = 0, oc = 0, pvc = 0;  // S_full, O_final, PV_done phases consumed
         bool ok = true;
         for (int k = 0; ok && k * G < p.num_items; ++k) {
             const int idx = snake_item(k, cta, G);
@@ -591,6 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < BN / 32; ++cc)
                     tmem_ld32(t_s + cc * 32, x + cc * 32);
                 tmem_wait_ld();
+                if (!C::kPAlias && j + 1 < nks) {
+                    // S_s is in registers: the MMA warp may compute the next S_s.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_s_free + 8 * s);
+                }
                 const int key0 = key_base + j * BN;
                 const bool need_mask = (key0 + BN > len) || (p.causal && key0 + BN - 1 > row - r);
                 if (need_mask) {
@@ -618,6 +729,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // p = exp2(S*c - m*c): packed FFMA2 for the arguments, SFU ex2,
                 // 8 independent partial row sums, bf16x2 packing into TMEM.
+                if (!C::kPAlias && j > 0) {
+                    // P_s(j-1) V is complete: P_s may be overwritten and O_s is
+                    // stable.  (With P aliasing S this is implied by S_full:
+                    // the next Q K^T was issued after that P V.)
+                    if (!warp_wait(bar_pv_done + 8 * s, pvc & 1, wc, 20 + s)) { ok = false; break; }
+                    ++pvc;
+                    tc_fence_after();
+                }
                 const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
                 const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
                 float2 rs4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -633,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rs4[i & 3] = __fadd2_rn(rs4[i & 3], e);
                         pk[i] = pack_bf16x2(e.x, e.y);
                     }
-                    tmem_st16(t_s + cc * 16, pk);
+                    tmem_st16(t_p + cc * 16, pk);
                 }
                 const float rs = ((rs4[0].x + rs4[0].y) + (rs4[1].x + rs4[1].y)) +
                                  ((rs4[2].x + rs4[2].y) + (rs4[3].x + rs4[3].y));
@@ -659,8 +778,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ------------------------------------------------- epilogue
-            if (!warp_wait(bar_o_final + 8 * s, oc & 1, wc, 18 + s)) { ok = false; break; }
-            ++oc;
+            if (C::kPAlias) {
+                if (!warp_wait(bar_o_final + 8 * s, oc & 1, wc, 18 + s)) { ok = false; break; }
+                ++oc;
+            } else {  // the last P V of the item
+                if (!warp_wait(bar_pv_done + 8 * s, pvc & 1, wc, 20 + s)) { ok = false; break; }
+                ++pvc;
+            }
             tc_fence_after();
             const bool live = l > 0.f;
             const float inv = live ? 1.f / l : 0.f;
