@@ -49,11 +49,14 @@ def _f64(x) -> np.ndarray:
 
 
 def _attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-            causal: bool, row_pos: np.ndarray, key_lo: int = 0, key_hi=None):
+            causal: bool, row_pos: np.ndarray, key_lo: int = 0, key_hi=None,
+            window=None):
     """One head of standard attention for the query rows ``q`` whose
     positions in the sequence are ``row_pos``, over the keys at positions
     ``key_lo <= j < key_hi`` only (all keys by default; the causal mask uses
-    absolute positions).
+    absolute positions).  ``window=(wl, wr)`` keeps key j for row i only if
+    ``i - wl <= j <= i + wr`` (a negative bound is unbounded) -- the local
+    band of DEMO 6, where ``|i - j| <= 64``.
 
     q: [r, d]; k, v: [n, d]; returns (O [r, d], L [r]) in float64.
     """
@@ -72,6 +75,12 @@ def _attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     s = np.where(outside[None, :], -np.inf, s)
     if causal:
         s = np.where(key_pos[None, :] > row_pos[:, None], -np.inf, s)
+    if window is not None:
+        wl, wr = window
+        if wl >= 0:
+            s = np.where(key_pos[None, :] < row_pos[:, None] - wl, -np.inf, s)
+        if wr >= 0:
+            s = np.where(key_pos[None, :] > row_pos[:, None] + wr, -np.inf, s)
     # STAGE 1: subtract the row max, exponentiate, normalise.
     m = s.max(axis=1)
     live = np.isfinite(m)
@@ -83,8 +92,9 @@ def _attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     return o, lse
 
 
-def attention_ref(q, k, v, scale: float, causal: bool):
-    """Standard attention over ``[..., N, D]`` inputs (any leading dims).
+def attention_ref(q, k, v, scale: float, causal: bool, window=None):
+    """Standard attention over ``[..., N, D]`` inputs (any leading dims),
+    optionally restricted to the local band ``window=(wl, wr)``.
 
     Returns ``(O [..., N, D], L [..., N])`` in float64.  One (N, N) float64
     score block exists at a time.
@@ -99,12 +109,13 @@ def attention_ref(q, k, v, scale: float, causal: bool):
     lse = np.empty((qf.shape[0], n))
     pos = np.arange(n)
     for h in range(qf.shape[0]):
-        o[h], lse[h] = _attend(qf[h], kf[h], vf[h], float(scale), causal, pos)
+        o[h], lse[h] = _attend(qf[h], kf[h], vf[h], float(scale), causal, pos,
+                               window=window)
     return o.reshape(*lead, n, vf.shape[-1]), lse.reshape(*lead, n)
 
 
 def attention_rows(q, k, v, scale: float, causal: bool, rows, key_lo: int = 0,
-                   key_hi=None):
+                   key_hi=None, window=None):
     """Standard attention for selected query rows of ONE head, optionally
     over a sub-range of the keys ``[key_lo, key_hi)`` (positions absolute).
 
@@ -114,7 +125,7 @@ def attention_rows(q, k, v, scale: float, causal: bool, rows, key_lo: int = 0,
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     rows = np.asarray(rows, dtype=np.int64)
-    return _attend(q[rows], k, v, float(scale), causal, rows, key_lo, key_hi)
+    return _attend(q[rows], k, v, float(scale), causal, rows, key_lo, key_hi, window)
 
 
 def merge_partials(o_parts, l_parts):

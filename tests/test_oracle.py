@@ -404,3 +404,61 @@ def test_merge_special_cases():
     # huge L values do not overflow
     O, L = merge_partials(np.stack([o[0], o[1]]), np.stack([l[0] + 800, l[1] + 810]))
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+
+
+# ---------------------------------------------------------------------------
+# the local band (DEMO 6's |i - j| <= 64, and general (wl, wr) windows)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("window", [(0, 0), (1, 2), (3, 0), (0, 5), (-1, 1), (2, -1)])
+def test_window_brute_force(window):
+    r = _rng(40)
+    n, d = 8, 3
+    q, k, v = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, 2))
+    wl, wr = window
+    O, L = attention_ref(q, k, v, 0.6, False, window=window)
+    for i in range(n):
+        keys = [j for j in range(n) if (wl < 0 or j >= i - wl) and (wr < 0 or j <= i + wr)]
+        w = [math.exp(0.6 * math.fsum(q[i][t] * k[j][t] for t in range(d))) for j in keys]
+        z = math.fsum(w)
+        assert abs(L[i] - math.log(z)) <= 1e-14
+        for c in range(2):
+            assert abs(O[i][c] - math.fsum(w[x] * v[j][c] for x, j in enumerate(keys)) / z) <= 1e-14
+
+
+def test_window_closed_forms():
+    r = _rng(41)
+    n, d = 50, 8
+    q, k, v = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, d))
+    # (0, 0): every row sees only its own key: O = V, L = scale q.k
+    O, L = attention_ref(q, k, v, 0.3, False, window=(0, 0))
+    assert np.max(np.abs(O - v)) <= 1e-14
+    assert np.max(np.abs(L - 0.3 * np.sum(q * k, axis=1))) <= 1e-13
+    # (-1, 0) is the causal mask; (-1, -1) is no mask
+    Oc, Lc = attention_ref(q, k, v, 0.3, True)
+    Ow, Lw = attention_ref(q, k, v, 0.3, False, window=(-1, 0))
+    assert np.array_equal(Oc, Ow) and np.array_equal(Lc, Lw)
+    Of, Lf = attention_ref(q, k, v, 0.3, False)
+    Ow, Lw = attention_ref(q, k, v, 0.3, False, window=(-1, -1))
+    assert np.array_equal(Of, Ow) and np.array_equal(Lf, Lw)
+    # Q = 0 under a band: O = mean of the V rows inside the band
+    O, L = attention_ref(np.zeros((n, d)), k, v, 0.3, False, window=(3, 5))
+    for i in range(n):
+        lo, hi = max(0, i - 3), min(n, i + 6)
+        assert np.allclose(O[i], v[lo:hi].mean(0), atol=1e-13)
+        assert abs(L[i] - math.log(hi - lo)) <= 1e-13
+
+
+def test_window_demo6_band():
+    """DEMO 6's local window: softmax over |i - j| <= 64 only -- a different
+    function from exact attention (the page's point), equal to the band
+    written out as a mask."""
+    r = _rng(42)
+    n, d = 512, 64
+    q, k, v = r.normal(size=(n, d)) / 8, r.normal(size=(n, d)) / 8, r.normal(size=(n, d))
+    O, _ = attention_ref(q, k, v, 1.0, False, window=(64, 64))
+    s = q @ k.T
+    band = np.abs(np.subtract.outer(np.arange(n), np.arange(n))) <= 64
+    e = np.exp(np.where(band, s, -np.inf) - np.where(band, s, -np.inf).max(1, keepdims=True))
+    assert np.max(np.abs(O - (e / e.sum(1, keepdims=True)) @ v)) <= 1e-13
+    Of, _ = attention_ref(q, k, v, 1.0, False)
+    assert np.max(np.abs(O - Of)) > 1e-3          # not the same function

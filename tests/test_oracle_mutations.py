@@ -76,8 +76,10 @@ MUTATIONS = ["transpose_qk", "no_scale", "scale_squared", "mask_flipped",
 
 
 def _run_pins(monkeypatch, mut):
-    monkeypatch.setattr(oa, "_attend",
-                        lambda *a: _attend_copy(*a, mut=mut))
+    def patched(*a, window=None):
+        assert window is None  # the pins use no band
+        return _attend_copy(*a, mut=mut)
+    monkeypatch.setattr(oa, "_attend", patched)
     failed = []
     for pin in ALL_PINS:
         try:
