@@ -26,7 +26,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
     "FA_ERR_DEVICE_TIMEOUT", "FA_F32", "FA_BF16", "FA_BF16_OUT_F32",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_TC", "FaError",
-    "load_library", "library_path", "fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
+    "load_library", "library_path", "fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
@@ -38,7 +38,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, \
 FA_F32, FA_BF16, FA_BF16_OUT_F32 = 0, 1, 2
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_splitkv",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
                     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc",
                     "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
@@ -84,6 +84,9 @@ def load_library():
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32,
                            i32, vp]
     lib.fa_fwd.restype = i32
+    lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32,
+                                  i32, i32, vp]
+    lib.fa_fwd_window.restype = i32
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                   i32, f32, i32, i32, vp]
     lib.fa_fwd_varlen.restype = i32
@@ -140,6 +143,14 @@ def fa_fwd(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, stream=None) -> int:
     return load_library().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L),
                                  int(B), int(H), int(N), int(D), float(scale),
                                  int(causal), int(dtype), _stream(stream))
+
+
+def fa_fwd_window(Q, K, V, O, L, B, H, N, D, scale, window_left, window_right, dtype,
+                  stream=None) -> int:
+    return load_library().fa_fwd_window(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L),
+                                        int(B), int(H), int(N), int(D), float(scale),
+                                        int(window_left), int(window_right), int(dtype),
+                                        _stream(stream))
 
 
 def fa_fwd_varlen(Q, K, V, O, L, cu_seqlens, num_seqs, total_tokens,

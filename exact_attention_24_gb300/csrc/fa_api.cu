@@ -134,9 +134,9 @@ fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns, cudaStre
 
 extern "C" {
 
-fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B,
-                 int H, int N, int D, float scale, int causal, fa_dtype dtype,
-                 fa_stream_t stream) {
+static fa_status fwd_dense(const void *Q, const void *K, const void *V, void *O, float *L, int B,
+                           int H, int N, int D, float scale, int causal, int wl, int wr,
+                           fa_dtype dtype, fa_stream_t stream) {
     if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
     const int64_t heads = (int64_t)B * H;
     fa_status st = check_common(Q, K, V, O, L, heads, N, D, scale, causal, dtype);
@@ -158,9 +158,23 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L,
     p.D = D;
     p.scale = scale;
     p.causal = causal;
+    p.wl = wl;
+    p.wr = wr;
     p.dtype = dtype;
     p.stream = static_cast<cudaStream_t>(stream);
     return dispatch(p);
+}
+
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
+                 int N, int D, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+    return fwd_dense(Q, K, V, O, L, B, H, N, D, scale, causal, -1, causal ? 0 : -1, dtype, stream);
+}
+
+fa_status fa_fwd_window(const void *Q, const void *K, const void *V, void *O, float *L, int B,
+                        int H, int N, int D, float scale, int window_left, int window_right,
+                        fa_dtype dtype, fa_stream_t stream) {
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    return fwd_dense(Q, K, V, O, L, B, H, N, D, scale, 0, window_left, window_right, dtype, stream);
 }
 
 fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *L,
@@ -191,6 +205,8 @@ fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, fl
     p.D = D;
     p.scale = scale;
     p.causal = causal;
+    p.wl = -1;
+    p.wr = causal ? 0 : -1;
     p.dtype = dtype;
     p.stream = static_cast<cudaStream_t>(stream);
     return dispatch(p);
@@ -232,6 +248,8 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
     p.D = D;
     p.scale = scale;
     p.causal = causal;
+    p.wl = -1;
+    p.wr = causal ? 0 : -1;
     p.dtype = dtype;
     p.num_splits = splits;
     p.workspace = workspace;

@@ -27,6 +27,7 @@ struct FaProblem {
     int D;
     float scale;
     int causal;
+    int wl, wr;       // key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     int dtype;        // fa_dtype
     uint32_t *err;    // device error word
     int grid_ctas;    // 0 = one per SM

@@ -38,6 +38,7 @@ struct SimtParams {
     int64_t total;
     float scale;
     int causal;
+    int wl, wr;  // key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     uint32_t *err;
 };
 
@@ -121,8 +122,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int t = 0; t < DC; ++t) acc[r][t] = 0.f;
     }
 
-    const int kv_end = p.causal ? min(len, q0 + kBr) : len;
-    for (int kv0 = 0; kv0 < kv_end; kv0 += kBc) {
+    // Keys any row of this block can see: [kv_lo, kv_end).
+    const int kv_end = p.wr >= 0 ? min(len, q0 + kBr - 1 + p.wr + 1) : len;
+    const int kv_lo = p.wl >= 0 ? max(0, q0 - p.wl) / kBc * kBc : 0;
+    for (int kv0 = kv_lo; kv0 < kv_end; kv0 += kBc) {
         __syncthreads();  // previous tile fully consumed (and sQ written)
         load_tile<D>(sK, D + 1, K, stride, kv0, len);
         load_tile<D>(sV, D, V, stride, kv0, len);
@@ -145,8 +148,10 @@ __global__ void __launch_bounds__(kWarps * 32)
             s0 *= p.scale;  // scale after the dot product
             s1 *= p.scale;
             const int key0 = kv0 + lane, key1 = kv0 + lane + 32;
-            if (key0 >= len || (p.causal && key0 > qi)) s0 = -INFINITY;
-            if (key1 >= len || (p.causal && key1 > qi)) s1 = -INFINITY;
+            const int hi = p.wr >= 0 ? qi + p.wr : len - 1;   // last visible key
+            const int lo = p.wl >= 0 ? qi - p.wl : 0;          // first visible key
+            if (key0 >= len || key0 > hi || key0 < lo) s0 = -INFINITY;
+            if (key1 >= len || key1 > hi || key1 < lo) s1 = -INFINITY;
             const float m_new = fmaxf(m[r], warp_max(fmaxf(s0, s1)));
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = (m[r] == -INFINITY) ? 0.f : expf(m[r] - m_use);
@@ -202,6 +207,8 @@ fa_status launch(const FaProblem &pr) {
     p.total = pr.total;
     p.scale = pr.scale;
     p.causal = pr.causal;
+    p.wl = pr.wl;
+    p.wr = pr.wr;
     p.err = pr.err;
     const size_t smem = sizeof(float) * (size_t)(kBr * D + kBc * (D + 1) + kBc * D);
     auto kern = fa_simt_kernel<D, Tin, Tout>;

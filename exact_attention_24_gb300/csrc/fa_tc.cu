@@ -106,6 +106,7 @@ struct TcParams {
     float scale;
     float scale_log2;  // scale * log2(e)
     int causal;
+    int wl, wr;        // key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     uint32_t *err;
     uint64_t wait_limit_ns;
 };
@@ -122,8 +123,9 @@ struct Item {
     int mb;          // 256-row block index
     int g;           // key-range split of the block
     int t0;          // first K/V tile of the split
-    int nk0, nk1;    // K/V tiles (from t0) needed by query tile 0 / 1 (0 = none)
-    int nkv;         // max(nk0, nk1)
+    int a0, a1;      // first K/V tile (relative to t0) of query tile 0 / 1
+    int nk0, nk1;    // end (exclusive, relative to t0) of the tiles of query tile 0 / 1
+    int nkv;         // max(nk0, nk1): tiles loaded for the item
 };
 
 // K/V tile range of split g of a block whose two query tiles need nk0_full and
@@ -139,8 +141,13 @@ __host__ __device__ __forceinline__ void split_range(int nk0_full, int nk1_full,
     nk1 = e1 > 0 ? e1 : 0;
 }
 
+__device__ __forceinline__ int snake_item(int round, int cta, int G) {
+    return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+}
+
 // Tiles needed from tile 0 by the two query tiles of block mb (rows
-// [256 mb, 256 mb + 256)) of a sequence of `len` rows.
+// [256 mb, 256 mb + 256)) of a sequence of `len` rows, causal or full: the
+// no-left-bound case of block_ranges, in closed form.
 __host__ __device__ __forceinline__ void block_tiles(int len, int mb, int causal, int &nk0, int &nk1) {
     const int row0 = mb * 256;
     const int tiles = (len + 127) / 128;
@@ -153,8 +160,55 @@ __host__ __device__ __forceinline__ void block_tiles(int len, int mb, int causal
     }
 }
 
-__device__ __forceinline__ int snake_item(int round, int cta, int G) {
-    return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+// K/V tile ranges [lo_s, hi_s) needed by the two query tiles of block mb
+// when key j is visible to row i iff i - wl <= j <= i + wr (a negative bound
+// is unbounded; causal is (-1, 0), no mask (-1, -1)).  An empty query tile
+// gets lo = hi = 0.  Because wl + wr >= 0, the two ranges touch: every tile in
+// [lo_0, hi_1) is read by at least one query tile.
+__host__ __device__ __forceinline__ void block_ranges(int len, int mb, int wl, int wr, int &lo0, int &hi0,
+                                                      int &lo1, int &hi1) {
+    int lo[2], hi[2];
+    for (int s = 0; s < 2; ++s) {
+        const int r0 = mb * 256 + s * 128;
+        if (r0 >= len) {
+            lo[s] = hi[s] = 0;
+            continue;
+        }
+        const int r1 = (r0 + 127 < len - 1) ? r0 + 127 : len - 1;
+        const int klo = wl < 0 ? 0 : (r0 - wl > 0 ? r0 - wl : 0);
+        const int khi = wr < 0 ? len - 1 : (r1 + wr < len - 1 ? r1 + wr : len - 1);
+        lo[s] = klo / 128;
+        hi[s] = khi / 128 + 1;
+    }
+    lo0 = lo[0];
+    hi0 = hi[0];
+    lo1 = lo[1];
+    hi1 = hi[1];
+}
+
+// Fill the tile ranges of an (unsplit) item.
+template <bool WIN>
+__device__ __forceinline__ void item_ranges(const TcParams &p, Item &it) {
+    if (!WIN) {
+        it.t0 = 0;
+        it.a0 = it.a1 = 0;
+        block_tiles(it.len, it.mb, p.causal, it.nk0, it.nk1);
+        it.nkv = max(it.nk0, it.nk1);
+        return;
+    }
+    int lo0, hi0, lo1, hi1;
+    block_ranges(it.len, it.mb, p.wl, p.wr, lo0, hi0, lo1, hi1);
+    it.t0 = lo0;
+    it.a0 = 0;
+    it.nk0 = hi0 - lo0;
+    if (hi1 > lo1) {
+        it.a1 = lo1 - lo0;
+        it.nk1 = hi1 - lo0;
+    } else {
+        it.a1 = 0;
+        it.nk1 = 0;
+    }
+    it.nkv = max(it.nk0, it.nk1);
 }
 
 // Decode item `idx`; returns false when the item holds no work.  Items are
@@ -172,6 +226,7 @@ struct Sched {
 // Varlen compact order: level L from the top, then the sequences that reach
 // L (longest first), then heads -- only items that hold work, so the snake
 // assignment spreads real work evenly instead of walking empty slots.
+template <bool WIN>
 __device__ __forceinline__ bool decode_varlen_compact(const TcParams &p, const Sched &sc, int idx,
                                                       Item &it) {
     int L = p.num_mblk - 1;
@@ -192,18 +247,13 @@ __device__ __forceinline__ bool decode_varlen_compact(const TcParams &p, const S
     it.start = start;
     it.len = len;
     if (it.mb * 2 * BM >= it.len) return false;
-    int nk0_full, nk1_full;
-    block_tiles(it.len, it.mb, p.causal, nk0_full, nk1_full);
-    it.t0 = 0;
-    it.nk0 = nk0_full;
-    it.nk1 = nk1_full;
-    it.nkv = max(it.nk0, it.nk1);
+    item_ranges<WIN>(p, it);
     return it.nkv > 0;
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool WIN>
 __device__ __forceinline__ bool decode_item(const TcParams &p, const Sched &sc, int idx, Item &it) {
-    if (!SPLIT && p.compact) return decode_varlen_compact(p, sc, idx, it);
+    if (!SPLIT && p.compact) return decode_varlen_compact<WIN>(p, sc, idx, it);
     const int S = SPLIT ? p.num_splits : 1;
     const int per_blk = p.units_bh * S;
     const int blk_from_end = idx / per_blk;
@@ -227,16 +277,15 @@ __device__ __forceinline__ bool decode_item(const TcParams &p, const Sched &sc, 
         it.len = p.n;
     }
     if (it.mb * 2 * BM >= it.len) return false;
-    int nk0_full, nk1_full;
-    block_tiles(it.len, it.mb, p.causal, nk0_full, nk1_full);
-    if (SPLIT) {
+    if (SPLIT) {  // split mode has no window: every range starts at tile 0
+        int nk0_full, nk1_full;
+        block_tiles(it.len, it.mb, p.causal, nk0_full, nk1_full);
         split_range(nk0_full, nk1_full, it.g, S, it.t0, it.nk0, it.nk1);
+        it.a0 = it.a1 = 0;
+        it.nkv = max(it.nk0, it.nk1);
     } else {
-        it.t0 = 0;
-        it.nk0 = nk0_full;
-        it.nk1 = nk1_full;
+        item_ranges<WIN>(p, it);
     }
-    it.nkv = max(it.nk0, it.nk1);
     return it.nkv > 0;
 }
 
@@ -305,7 +354,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint6
 }
 
 // --------------------------------------------------------------- kernel --
-template <int D, int OUT>
+template <int D, int OUT, bool WIN>
 // 10 warps put 3 warps on two of the four SM sub-partitions, whose register
 // files hold 16K registers each: at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -336,6 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + C::kBarBytes - 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Band masks with a left bound exist only in the WIN instantiation; the
+    // plain causal / full kernels keep the simpler fixed-start schedule.
+    const int win_l = WIN ? p.wl : -1;
 
     if (warp == kProducerWarp && lane == 0) {
         mbar_init(bar_q_full, 1);
@@ -413,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int idx = snake_item(k, cta, G);
                 if (idx >= p.num_items) continue;
                 Item it;
-                if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
+                if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
                 if (items > 0 && !mbar_wait(bar_q_empty, (items - 1) & 1, wc, 1)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar_q_full, 2 * C::kTileBytes);
                 for (int s = 0; s < 2; ++s) {
@@ -476,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int idx = snake_item(k, cta, G);
                 if (idx >= p.num_items) continue;
                 Item it;
-                if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
+                if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
                 if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
                 ++items;
                 tc_fence_after();
@@ -486,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     const uint64_t dk0 = dk_ring + (l0 % C::kSlots) * kSlotDesc;
-                    issue_qk<D>(t_s0, dq0, dk0);
+                    issue_qk<D>(t_s0, dq0, dk0);  // query tile 0 always starts at t0
                     mma_commit(bar_s_full);
-                    if (it.nk1 > 0) {
+                    if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
                         issue_qk<D>(t_s1, dq1, dk0);
                         mma_commit(bar_s_full + 8);
                     }
@@ -498,7 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 for (int j = 0; j < it.nkv; ++j) {
                     const uint32_t li_v = l0 + 2 * j + 1, li_kn = li_v + 1;
-                    const bool need0 = j + 1 < it.nk0, need1 = j + 1 < it.nk1;
+                    // query tile s reads K/V tiles [a_s, nk_s); a tile that starts
+                    // at j + 1 has no softmax of tile j to wait for
+                    const bool need0 = j + 1 < it.nk0, need1 = j + 1 < it.nk1 && j + 1 >= (WIN ? it.a1 : 0);
                     if (need0 || need1) {
                         if (!ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8)) { ok = false; break; }
                         const uint64_t dkn = dk_ring + (li_kn % C::kSlots) * kSlotDesc;
@@ -513,8 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                         }
                         if (need1) {
-                            if (!warp_wait(bar_s_free + 8, fc1 & 1, wc, 11)) { ok = false; break; }
-                            ++fc1;
+                            if (j >= (WIN ? it.a1 : 0)) {
+                                if (!warp_wait(bar_s_free + 8, fc1 & 1, wc, 11)) { ok = false; break; }
+                                ++fc1;
+                            }
                             tc_fence_after();
                             if (elect_one()) {
                                 issue_qk<D>(t_s1, dq1, dkn);
@@ -540,12 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                     }
-                    if (j < it.nk1) {
+                    if (j < it.nk1 && j >= (WIN ? it.a1 : 0)) {
                         if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
                         ++pc1;
                         tc_fence_after();
                         if (elect_one()) {
-                            issue_pv<D>(t_o1, t_p1, dv, j > 0 ? 1u : 0u);
+                            issue_pv<D>(t_o1, t_p1, dv, j > (WIN ? it.a1 : 0) ? 1u : 0u);
                             mma_commit(bar_pv_done + 8);
                         }
                         __syncwarp();
@@ -559,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
+            if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
             if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
             ++items;
             tc_fence_after();
@@ -571,9 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // prologue: S_s = Q_s K_0^T; K_0 is read only by these, release it.
             if (elect_one()) {
-                issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);
+                issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);  // tile 0 starts at t0
                 mma_commit(bar_s_full);
-                if (it.nk1 > 0) {
+                if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
                     issue_qk<D>(t_s1, dq1, dk_ring + s_k0 * kSlotDesc);
                     mma_commit(bar_s_full + 8);
                 }
@@ -613,8 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
-                // query tile 1
-                if (j < it.nk1) {
+                // query tile 1 (reads tiles [a1, nk1): with a left window bound it
+                // may start after tile 0)
+                if (j < it.nk1 && j >= (WIN ? it.a1 : 0)) {
                     if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
                     ++pc1;
                     const bool more = j + 1 < it.nk1;
@@ -626,13 +683,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_pv<D>(t_o1, t_s1, dv, j > 0 ? 1u : 0u);
+                        issue_pv<D>(t_o1, t_s1, dv, j > (WIN ? it.a1 : 0) ? 1u : 0u);
                         if (more) {
                             issue_qk<D>(t_s1, dq1, dkn);
                             mma_commit(bar_s_full + 8);
                         } else {
                             mma_commit(bar_o_final + 8);
                         }
+                    }
+                    __syncwarp();
+                } else if (j + 1 == (WIN ? it.a1 : 0) && it.nk1 > (WIN ? it.a1 : 0)) {
+                    // query tile 1 starts at tile j + 1: its first Q K^T
+                    if (!kn_ready &&
+                        !warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 9)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk<D>(t_s1, dq1, dkn);
+                        mma_commit(bar_s_full + 8);
                     }
                     __syncwarp();
                 }
@@ -668,12 +738,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
-            if (!decode_item<OUT == kOutPart>(p, sched, idx, it)) continue;
-            const int nks = s == 0 ? it.nk0 : it.nk1;
-            if (nks == 0) continue;
+            if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
+            const int a_s = s == 0 ? 0 : (WIN ? it.a1 : 0);
+            const int nks = (s == 0 ? it.nk0 : it.nk1) - a_s;  // tiles this query tile reads
+            if (nks <= 0) continue;
             const int row = it.mb * 2 * BM + s * BM + r;   // row within the sequence
             const int len = it.len;
-            const int key_base = it.t0 * BN;               // first key of this split
+            const int key_base = (it.t0 + a_s) * BN;       // first key this query tile reads
             const bool store = row < len;
             int64_t orow, li;                              // where O and L of this row go
             if (OUT == kOutPart) {  // dense only: [split][b*h][row]
@@ -703,12 +774,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(bar_s_free + 8 * s);
                 }
                 const int key0 = key_base + j * BN;
-                const bool need_mask = (key0 + BN > len) || (p.causal && key0 + BN - 1 > row - r);
+                // Rows of this query tile are row - r .. row - r + 127; a tile needs
+                // masking if it crosses the sequence end or a window edge.
+                const bool need_mask = (key0 + BN > len) ||
+                                       (p.wr >= 0 && key0 + BN - 1 > row - r + p.wr) ||
+                                       (win_l >= 0 && key0 < row - r + 127 - win_l);
                 if (need_mask) {
-                    const int lim = p.causal ? min(row + 1, len) : len;  // keys < lim are live
+                    // keys in [lo_lim, hi_lim) are live for this row
+                    const int hi_lim = p.wr >= 0 ? min(row + p.wr + 1, len) : len;
+                    const int lo_lim = win_l >= 0 ? row - win_l : 0;
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
-                        if (key0 + i >= lim) x[i] = -INFINITY;
+                        if (key0 + i >= hi_lim || key0 + i < lo_lim) x[i] = -INFINITY;
                 }
                 // Row max: 8 independent chains of 3-input max, then a tree.
                 float mx8[8];
@@ -940,7 +1017,7 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-template <int D, int OUT>
+template <int D, int OUT, bool WIN>
 fa_status launch(const FaProblem &pr, int splits) {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
@@ -984,12 +1061,14 @@ fa_status launch(const FaProblem &pr, int splits) {
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.causal = pr.causal;
+    p.wl = pr.wl;
+    p.wr = pr.wr;
     p.err = pr.err;
     p.wait_limit_ns = pr.wait_limit_ns;
     int grid = pr.grid_ctas > 0 ? pr.grid_ctas : num_sms();
     if (grid <= 0) return FA_ERR_CUDA;  // device query failed (recorded)
     if (grid > p.num_items) grid = p.num_items;
-    auto kern = fa_tc_kernel<D, OUT>;
+    auto kern = fa_tc_kernel<D, OUT, WIN>;
     cudaFuncAttributes fattr;
     cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return fa_cuda_fail(e);
@@ -1020,8 +1099,14 @@ fa_status launch_merge(const FaProblem &pr, int splits) {
 template <int D>
 fa_status launch_d(const FaProblem &pr) {
     const bool f32 = pr.dtype == FA_BF16_OUT_F32;
-    if (pr.num_splits <= 1) return f32 ? launch<D, kOutF32>(pr, 1) : launch<D, kOutBf16>(pr, 1);
-    const fa_status st = launch<D, kOutPart>(pr, pr.num_splits);
+    // Causal (-1, 0) and full (-1, -1) use the plain kernels; any other band
+    // the WIN instantiation.
+    const bool win = pr.wl >= 0 || pr.wr > 0;
+    if (pr.num_splits <= 1) {
+        if (win) return f32 ? launch<D, kOutF32, true>(pr, 1) : launch<D, kOutBf16, true>(pr, 1);
+        return f32 ? launch<D, kOutF32, false>(pr, 1) : launch<D, kOutBf16, false>(pr, 1);
+    }
+    const fa_status st = launch<D, kOutPart, false>(pr, pr.num_splits);
     if (st != FA_OK) return st;
     return f32 ? launch_merge<D, true>(pr, pr.num_splits) : launch_merge<D, false>(pr, pr.num_splits);
 }
@@ -1049,7 +1134,7 @@ bool fa_tc_split_plan(int units_bh, int n, int D, int requested, int &splits, si
 
 fa_status fa_launch_tc(const FaProblem &pr) {
     if (pr.dtype != FA_BF16 && pr.dtype != FA_BF16_OUT_F32) return FA_ERR_UNSUPPORTED;
-    if (pr.num_splits > 1 && pr.varlen) return FA_ERR_UNSUPPORTED;
+    if (pr.num_splits > 1 && (pr.varlen || pr.wl >= 0 || pr.wr > 0)) return FA_ERR_UNSUPPORTED;
     if (pr.D == 64) return fa::launch_d<64>(pr);
     if (pr.D == 128) return fa::launch_d<128>(pr);
     return FA_ERR_UNSUPPORTED;

@@ -103,6 +103,21 @@ FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O,
                  int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd_window -- dense batch restricted to a local band of keys: key j is
+ * visible to query i iff i - window_left <= j <= i + window_right, where -1
+ * leaves that side unbounded.  (-1, 0) is the causal mask, (-1, -1) no mask,
+ * and (64, 64) the local window that "FlashAttention -- for programmers, not
+ * researchers.", DEMO 6, contrasts with exact attention (|i - j| <= 64).
+ * Tiles wholly outside the band are never loaded.  Other arguments as fa_fwd.
+ *
+ *   window_left, window_right : >= -1 (FA_ERR_INVALID_ARG otherwise)
+ */
+FA_API fa_status fa_fwd_window(const void *Q, const void *K, const void *V, void *O,
+                               float *L, int B, int H, int N, int D, float scale,
+                               int window_left, int window_right, fa_dtype dtype,
+                               fa_stream_t stream);
+
+/*
  * fa_fwd_varlen -- packed batch of variable-length sequences (self
  * attention: queries and keys share cu_seqlens).
  *

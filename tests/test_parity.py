@@ -333,3 +333,71 @@ def test_splitkv_merge_agrees_with_oracle_merge():
              for a, b in zip(cuts[:-1], cuts[1:])]
     mo, ml = merge_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
     assert np.max(np.abs(mo - ref_o)) < 1e-12 and np.max(np.abs(ml - ref_l)) < 1e-12
+
+
+# ------------------------------------------------------------ local band --
+def run_window(q, k, v, wl, wr, code, scale):
+    B, H, N, D = q.shape
+    O = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16 if code == fa.FA_BF16 else torch.float32,
+                   device=q.device)
+    L = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
+    st = fa.fa_fwd_window(q, k, v, O, L, B, H, N, D, scale, wl, wr, code, None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    return O, L
+
+
+WINDOW_CASES = [(1, 2, 1000, 64, 64, 64), (1, 1, 777, 128, 100, 30), (2, 1, 600, 128, 0, 0),
+                (1, 1, 2048, 128, 300, -1), (1, 2, 1500, 64, 5, 200), (1, 1, 513, 64, 127, 129),
+                (1, 1, 1024, 128, 256, 0), (1, 1, 300, 128, 1000, 1000)]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_window_matches_oracle(kernel, case):
+    B, H, N, D, wl, wr = case
+    w, q, k, v = _dense_case(B, H, N, D, "bf16", False, seed=N + wl)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, False, window=(wl, wr))
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for code in BF16_CODES:
+        O, L = run_window(qd, kd, vd, wl, wr, code, w.scale)
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"{kernel} window {case} dt={code}")
+
+
+def test_window_demo6_band_f32(kernel):
+    """DEMO 6's local window |i - j| <= 64 at its own size (n = 512, d = 64),
+    float32 path."""
+    w, q, k, v = _dense_case(1, 1, 512, 64, "f32", False, seed=6)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, False, window=(64, 64))
+    O, L = run_window(q.to(DEV), k.to(DEV), v.to(DEV), 64, 64, fa.FA_F32, w.scale)
+    assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_F32, "DEMO 6 band")
+
+
+def test_window_special_cases_are_the_plain_paths(kernel):
+    w, q, k, v = _dense_case(1, 2, 1100, 128, "bf16", True, seed=8)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    Oc, Lc = run_dense(qd, kd, vd, True, fa.FA_BF16, w.scale)
+    Ow, Lw = run_window(qd, kd, vd, -1, 0, fa.FA_BF16, w.scale)
+    assert torch.equal(Oc, Ow) and torch.equal(Lc, Lw)
+    On, Ln = run_dense(qd, kd, vd, False, fa.FA_BF16, w.scale)
+    Ow, Lw = run_window(qd, kd, vd, -1, -1, fa.FA_BF16, w.scale)
+    assert torch.equal(On, Ow) and torch.equal(Ln, Lw)
+
+
+def test_window_full_size_sampled_rows():
+    """A causal local window (keys i-512 .. i) at the C3 shape."""
+    w = C3
+    q, k, v = make_inputs(w)
+    O, L = run_window(q.to(DEV), k.to(DEV), v.to(DEV), 512, 0, fa.FA_BF16_OUT_F32, w.scale)
+    for b, h in [(0, 0), (1, 15), (0, 7)]:
+        rows = sample_rows(w.N, 48, seed=b * 16 + h)
+        ref_o, ref_l = attention_rows(q[b, h], k[b, h], v[b, h], w.scale, False, rows, window=(512, 0))
+        assert_close(to_f64(O[b, h, rows]), to_f64(L[b, h, rows]), ref_o, ref_l,
+                     fa.FA_BF16_OUT_F32, f"band C3 b={b} h={h}")
+
+
+def test_window_argument_checks():
+    q = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device=DEV)
+    O = torch.zeros_like(q)
+    L = torch.zeros(1, 1, 16, device=DEV)
+    assert fa.fa_fwd_window(q, q, q, O, L, 1, 1, 16, 64, 0.1, -2, 0, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_window(q, q, q, O, L, 1, 1, 16, 64, 0.1, 0, -5, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
