@@ -538,8 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     const uint64_t dk0 = dk_ring + (l0 % C::kSlots) * kSlotDesc;
-                    issue_qk<D>(t_s0, dq0, dk0);  // query tile 0 always starts at t0
-                    mma_commit(bar_s_full);
+                    // Query tile 0's range starts at t0; in split mode it can be
+                    // empty (the last key range of a short causal block).
+                    if (it.nk0 > 0) {
+                        issue_qk<D>(t_s0, dq0, dk0);
+                        mma_commit(bar_s_full);
+                    }
                     if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
                         issue_qk<D>(t_s1, dq1, dk0);
                         mma_commit(bar_s_full + 8);
@@ -627,8 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // prologue: S_s = Q_s K_0^T; K_0 is read only by these, release it.
             if (elect_one()) {
-                issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);  // tile 0 starts at t0
-                mma_commit(bar_s_full);
+                // Query tile 0's range starts at t0; in split mode it can be
+                // empty (the last key range of a short causal block).
+                if (it.nk0 > 0) {
+                    issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);
+                    mma_commit(bar_s_full);
+                }
                 if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
                     issue_qk<D>(t_s1, dq1, dk_ring + s_k0 * kSlotDesc);
                     mma_commit(bar_s_full + 8);

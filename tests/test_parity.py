@@ -310,6 +310,26 @@ def test_splitkv_matches_oracle(case):
         assert_close(to_f64(O), to_f64(L), ref_o, ref_l, code, f"split {case} dt={code}")
 
 
+def test_splitkv_small_grid_runs_consecutive_items():
+    """With a small persistent grid each CTA runs many split items in a row,
+    among them items whose first query tile has no keys in its range (the
+    last of 16 key ranges of a short causal block) followed by items whose
+    first tile does.  Results match the oracle and do not depend on the grid."""
+    w, q, k, v = _dense_case(1, 2, 2048, 64, "bf16", True, seed=31)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, True)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    res = []
+    try:
+        for grid in (1, 3, 0):
+            fa.fa_set_options(fa.FA_KERNEL_AUTO, grid, 0)
+            res.append(run_splitkv(qd, kd, vd, True, fa.FA_BF16_OUT_F32, w.scale, 16))
+    finally:
+        fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+    for O, L in res:
+        assert_close(to_f64(O), to_f64(L), ref_o, ref_l, fa.FA_BF16_OUT_F32, "split, small grid")
+        assert torch.equal(O, res[-1][0]) and torch.equal(L, res[-1][1])
+
+
 def test_splitkv_one_split_is_the_dense_path():
     w, q, k, v = _dense_case(1, 2, 1500, 128, "bf16", True, seed=9)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
