@@ -23,6 +23,7 @@ path); the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -200,16 +201,14 @@ def bench_ours(args, w, rank, world, local):
     import torch
     import exact_attention_24_gb300 as fa
     from exact_attention_24_gb300.build import build
-    from exact_attention_24_gb300.workloads import Workload, make_inputs
+    from exact_attention_24_gb300.workloads import make_inputs
 
     build()
     fa.load_library()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    wr = Workload(w.name, w.B, w.H, w.N, w.D, w.dtype, w.causal,
-                  rank_seed(w.seed, rank), w.qk_mult, w.lengths)
-    q, k, v = make_inputs(wr)
+    q, k, v = make_inputs(dataclasses.replace(w, seed=rank_seed(w.seed, rank)))
     code = fa.FA_BF16
     in_bytes = 3 * q.numel() * q.element_size()
     out_b = q.numel() * 2 + q.numel() // w.D * 4
@@ -234,6 +233,9 @@ def bench_ours(args, w, rank, world, local):
         if args.splits is not None:
             st = fa.fa_fwd_splitkv(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
                                    code, args.splits, ws, ws_bytes, stream)
+        elif w.window:
+            st = fa.fa_fwd_window(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, w.window[0],
+                                  w.window[1], code, stream)
         elif w.varlen:
             st = fa.fa_fwd_varlen(qd, kd, vd, O, L, cu, len(w.lengths), w.total, w.max_seqlen,
                                   w.H, w.D, w.scale, int(w.causal), code, stream)
@@ -308,7 +310,20 @@ def bench_ours(args, w, rank, world, local):
     barrier(world)
     e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
-    peak, _, peak_kind = load_peaks()
+    peak, hbm_peak, peak_kind = load_peaks()
+    min_bytes = w.min_bytes(2)
+    t_launch = ms_local / args.steps * 1e-3
+    if min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
+        roofline = {"bound": "hbm", "achieved": round(min_bytes / t_launch / 1e9, 1),
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(min_bytes / t_launch / 1e9 / hbm_peak, 4),
+                     "peak_source": f"hbm_gbs of {peak_kind}"}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4),
+                    "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
+    roofline["traffic"] = load_traffic("fa_tc", w.name)
     rec = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -323,18 +338,18 @@ def bench_ours(args, w, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
-                   "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
+                   "causal": w.causal, "window": list(w.window) or None,
+                   "out_dtype": "bf16", "seed": w.seed,
                    "lengths": list(w.lengths) if w.varlen else None,
                    "splits": args.splits,
                    "flops_per_step": flops,
                    "l2": f"inputs rotated over {copies} resident copies "
                          f"({copies * (in_bytes + out_b) / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4),
-                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
-                     "traffic": load_traffic("fa_tc", w.name)},
+        "roofline": roofline,
+        "io": {"min_bytes": min_bytes,
+               "tile_model_bytes": io_model_bytes(w, 256, 128),
+               "tile_model_bytes_64x64": io_model_bytes(w, 64, 64)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": in_bytes,
                 "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
@@ -343,6 +358,31 @@ def bench_ours(args, w, rank, world, local):
         "clocks": sampler.summary(),
     }
     return rec
+
+
+# -------------------------------------------------------------- IO model --
+def io_model_bytes(w, br: int, bc: int) -> int:
+    """HBM bytes of the tiled loop under the byte-counting rule of
+    "FlashAttention -- for programmers, not researchers.", STAGE 0 and
+    STAGE 4: per head, each br-row query block loads its Q rows once and
+    every bc-key K/V tile it needs, then writes its O rows once; nothing is
+    cached between blocks.  Here with the workload's element size, only the
+    key tiles that the mask leaves visible to some row of the block, and
+    the 4-byte L per row that the page's counter leaves out."""
+    import numpy as np
+    e = 4 if w.dtype == "f32" else 2
+    lens = w.lengths if w.varlen else (w.N,) * w.B
+    total = 0
+    for n in lens:
+        kv_rows = 0
+        for r0 in range(0, n, br):
+            lo, hi = w.visible_range(np.arange(r0, min(n, r0 + br)), n)
+            live = hi >= lo
+            if live.any():
+                first = int(lo[live].min()) // bc * bc
+                kv_rows += min(n, (int(hi[live].max()) // bc + 1) * bc) - first
+        total += w.H * (e * (2 * n * w.D + 2 * kv_rows * w.D) + 4 * n)
+    return int(total)
 
 
 # --------------------------------------------------------- CPU oracle arm --
@@ -369,13 +409,14 @@ def oracle_rows_sample(w, view, rows: int, seed: int):
     n = view[0].shape[0]
     rng = np.random.default_rng(seed)
     picks = np.sort(rng.choice(n, size=min(rows, n), replace=False))
-    keys = (picks + 1) if w.causal else np.full(picks.shape, n)
+    keys = w.visible_keys(picks, n)
     return picks, float(np.sum(4.0 * keys * w.D))
 
 
 def run_oracle_sample(w, view, picks):
     from oracle import attention_rows
-    attention_rows(view[0], view[1], view[2], w.scale, w.causal, picks)
+    attention_rows(view[0], view[1], view[2], w.scale, w.causal, picks,
+                   window=tuple(w.window) or None)
 
 
 def _f64_views(w):
@@ -441,7 +482,7 @@ def bench_reference(args, w, rank, world):
         "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
-                   "causal": w.causal},
+                   "causal": w.causal, "window": list(w.window) or None},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -457,14 +498,25 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="B2_H16_N4096_D128_bf16_causal")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of oracle time for cpu_baseline (0 = leave it out)")
     ap.add_argument("--splits", type=int, default=None,
                     help="time fa_fwd_splitkv with this many key splits (0 = automatic)")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,D[,causal] instead of a named workload (bf16, seed 8)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    from exact_attention_24_gb300.workloads import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from exact_attention_24_gb300.workloads import WORKLOADS, Workload
+    if args.shape:
+        f = [int(x) for x in args.shape.split(",")]
+        if len(f) not in (4, 5):
+            ap.error("--shape wants B,H,N,D[,causal]")
+        causal = bool(f[4]) if len(f) == 5 else False
+        name = f"B{f[0]}_H{f[1]}_N{f[2]}_D{f[3]}_bf16" + ("_causal" if causal else "")
+        w = Workload(name, f[0], f[1], f[2], f[3], "bf16", causal, 8)
+    else:
+        w = WORKLOADS[args.workload]
     rank, world, local = dist_env()
     if world != args.gpus:
         world = max(world, 1)
@@ -480,7 +532,8 @@ def main(argv=None):
     rec = bench_ours(args, w, rank, world, local)
     if rank == 0:
         if world == 1:
-            rec["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            rec["cpu_baseline"] = (cpu_baseline(w, args.cpu_seconds)
+                                   if args.cpu_seconds > 0 else None)
         print(json.dumps(rec), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -38,7 +38,8 @@ class Workload:
     Dense workloads have ``B, H, N, D`` and layout ``[B, H, N, D]``.
     Variable-length workloads have ``lengths`` (one per sequence) and layout
     ``[total, H, D]`` with ``cu_seqlens`` prefix offsets; ``B``/``N`` are then
-    unused.
+    unused.  ``window=(wl, wr)`` (dense only) restricts query i to the keys
+    ``i - wl .. i + wr``, -1 leaving a side unbounded.
     """
 
     name: str
@@ -51,6 +52,7 @@ class Workload:
     seed: int
     qk_mult: float = 1.0
     lengths: tuple = field(default=())
+    window: tuple = field(default=())
 
     @property
     def varlen(self) -> bool:
@@ -72,9 +74,36 @@ class Workload:
     def max_seqlen(self) -> int:
         return int(max(self.lengths)) if self.varlen else self.N
 
+    def visible_range(self, rows, n: int):
+        """First and last key position (lo, hi) that each query row of a
+        sequence of n attends to under the workload's mask; hi < lo when
+        none."""
+        rows = np.asarray(rows, dtype=np.int64)
+        lo = np.zeros_like(rows)
+        hi = np.full_like(rows, n - 1)
+        if self.causal:
+            hi = np.minimum(hi, rows)
+        if self.window:
+            wl, wr = self.window
+            if wl >= 0:
+                lo = np.maximum(lo, rows - wl)
+            if wr >= 0:
+                hi = np.minimum(hi, rows + wr)
+        return lo, hi
+
+    def visible_keys(self, rows, n: int) -> np.ndarray:
+        """Number of keys each query row attends to under the mask."""
+        lo, hi = self.visible_range(rows, n)
+        return np.maximum(hi - lo + 1, 0)
+
     def flops(self) -> float:
         """Algorithmic FLOPs: two (n x n x d) contractions at 2 flops per
-        multiply-add, i.e. 4 n^2 d per head, halved under the causal mask."""
+        multiply-add, i.e. 4 n^2 d per head, halved under the causal mask
+        (the benchmark's stated convention).  Under a band window: 4 d per
+        (query, key) pair that the band keeps."""
+        if self.window:
+            pairs = float(self.visible_keys(np.arange(self.N), self.N).sum())
+            return 4.0 * self.B * self.H * self.D * pairs
         f = 0.5 if self.causal else 1.0
         if self.varlen:
             return sum(4.0 * self.H * n * n * self.D * f for n in self.lengths)
@@ -124,4 +153,12 @@ C5 = Workload("varlen16_H16_D128_bf16_causal", 0, 16, 0, 128, "bf16", True,
 # head x 2 heads = 128 work items for 152 SMs, the case split keys are for.
 SPLIT_LONG = Workload("B1_H2_N16384_D128_bf16_causal", 1, 2, 16384, 128, "bf16", True, 5)
 
-WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C5, SPLIT_LONG)}
+# The local band |i - j| <= 64 that the exactness demo contrasts with exact
+# attention, at the shape of C3.
+BAND64 = Workload("B2_H16_N4096_D128_bf16_band64", 2, 16, 4096, 128, "bf16", False, 6,
+                  window=(64, 64))
+# A causal sliding window of 4096 keys over a 32K-token context.
+SLIDING4K = Workload("B1_H16_N32768_D128_bf16_sliding4096", 1, 16, 32768, 128, "bf16", False, 7,
+                     window=(4096, 0))
+
+WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C5, SPLIT_LONG, BAND64, SLIDING4K)}

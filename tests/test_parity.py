@@ -17,7 +17,7 @@ import torch
 
 import exact_attention_24_gb300 as fa
 from exact_attention_24_gb300 import build as fa_build
-from exact_attention_24_gb300.workloads import (C1, C2, C3, C4, C5, Workload,
+from exact_attention_24_gb300.workloads import (C1, C2, C3, C4, C5, WORKLOADS, Workload,
                                                 default_scale, make_inputs)
 from helpers import (assert_close, run_dense, run_varlen, sample_rows, to_f64)
 from oracle import attention_ref, attention_ref_varlen, attention_rows
@@ -413,6 +413,24 @@ def test_window_full_size_sampled_rows():
         ref_o, ref_l = attention_rows(q[b, h], k[b, h], v[b, h], w.scale, False, rows, window=(512, 0))
         assert_close(to_f64(O[b, h, rows]), to_f64(L[b, h, rows]), ref_o, ref_l,
                      fa.FA_BF16_OUT_F32, f"band C3 b={b} h={h}")
+
+
+@pytest.mark.parametrize("name", ["B2_H16_N4096_D128_bf16_band64",
+                                  "B1_H16_N32768_D128_bf16_sliding4096"])
+def test_window_bench_workloads_sampled_rows(name):
+    """The band workloads the benchmark times, at full size and in the same
+    launch (bf16 O), on sampled rows."""
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    O, L = run_window(q.to(DEV), k.to(DEV), v.to(DEV), w.window[0], w.window[1], fa.FA_BF16,
+                      w.scale)
+    assert not torch.isnan(O.float()).any() and not torch.isnan(L).any()
+    for b, h in [(0, 0), (w.B - 1, w.H - 1), (0, w.H // 2)]:
+        rows = sample_rows(w.N, 40, seed=b * 16 + h)
+        ref_o, ref_l = attention_rows(q[b, h], k[b, h], v[b, h], w.scale, False, rows,
+                                      window=w.window)
+        assert_close(to_f64(O[b, h, rows]), to_f64(L[b, h, rows]), ref_o, ref_l, fa.FA_BF16,
+                     f"{name} b={b} h={h}")
 
 
 def test_window_argument_checks():
