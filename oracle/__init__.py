@@ -1,4 +1,5 @@
-"""CPU oracle for the FlashAttention-2 forward pass -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the FlashAttention-2 forward and backward passes -- TEST
+INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import anything from this package.  The product path
@@ -21,8 +22,17 @@ The oracle is written from the definition of attention, in float64 NumPy:
   one-pass definition (block-size invariance) and to show that the
   no-rescale variant of STAGE 4 is wrong.
 
-Every function here is pinned by ``tests/test_oracle.py`` against closed
-forms, brute force in pure Python, and ``torch`` CPU library routines.
+* ``attention_bwd_ref`` / ``attention_bwd_ref_varlen`` -- the gradients of
+  ``sum(O * dO)`` from the plain definition (explicit P, the softmax
+  derivative dS = P (dP - rowsum(dO O))), in the five contractions that
+  "FlashAttention" (dao-ailab docs page), "Application in Backward Pass
+  (5 MMAs)", lists.
+* ``attention_bwd_recompute`` -- the same gradients by STAGE 5's route:
+  P recomputed tile by tile from Q, K and the stored L.
+
+Every function here is pinned by ``tests/test_oracle.py`` and
+``tests/test_oracle_bwd.py`` against closed forms, brute force in pure
+Python, finite differences and ``torch`` CPU library routines.
 """
 
 from .attention import (  # noqa: F401
@@ -31,4 +41,10 @@ from .attention import (  # noqa: F401
     attention_tiled,
     attention_rows,
     merge_partials,
+)
+from .backward import (  # noqa: F401
+    attention_bwd_recompute,
+    attention_bwd_ref,
+    attention_bwd_ref_varlen,
+    forward_for_backward,
 )
