@@ -30,7 +30,8 @@ __all__ = [
     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
-    "attention_varlen", "EXPORTED_SYMBOLS",
+    "attention_varlen", "EXPORTED_SYMBOLS", "fa_bwd", "fa_bwd_workspace_size",
+    "attention_bwd",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, \
@@ -40,7 +41,7 @@ FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
                     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc",
-                    "fa_check_device_error",
+                    "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
                     "fa_get_options", "fa_watchdog_selftest")
 
@@ -98,6 +99,11 @@ def load_library():
     lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
                                            i32, i32, i32, vp]
     lib.fa_fwd_splitkv_noalloc.restype = i32
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32,
+                           i32, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd.restype = i32
+    lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -187,6 +193,18 @@ def fa_fwd_splitkv_workspace_size(B, H, N, D, num_splits) -> int:
                                                             int(num_splits)))
 
 
+def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, D, scale, causal, dtype, workspace,
+           workspace_bytes, stream=None) -> int:
+    return load_library().fa_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
+        int(B), int(H), int(N), int(D), float(scale), int(causal), int(dtype), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_workspace_size(B, H, N) -> int:
+    return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N)))
+
+
 def fa_check_device_error(stream=None) -> int:
     return load_library().fa_check_device_error(_stream(stream))
 
@@ -247,6 +265,26 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None,
     if st != FA_OK:
         raise FaError(st, "fa_fwd" if num_splits is None else "fa_fwd_splitkv")
     return O, L
+
+
+def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+                  out_dtype=None, stream=None):
+    """dQ, dK, dV for ``[B, H, N, D]`` CUDA tensors, given the forward
+    pass's O and L (``attention``'s outputs) and dO; the workspace is
+    allocated here with torch."""
+    import torch
+    B, H, N, D = q.shape
+    code, odt = _dtype_code(q, out_dtype)
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+    grads = [torch.empty((B, H, N, D), dtype=odt, device=q.device) for _ in range(3)]
+    nbytes = fa_bwd_workspace_size(B, H, N)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, o, do, lse, *grads, B, H, N, D, scale, int(causal), code, ws, nbytes,
+                stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return tuple(grads)
 
 
 def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,

@@ -272,6 +272,84 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int D, int num_splits)
     return need;
 }
 
+size_t fa_bwd_workspace_size(int B, int H, int N) {
+    if (B <= 0 || H <= 0 || N <= 0) return 0;
+    const size_t rows = (size_t)B * (size_t)H * (size_t)N;
+    return (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                 float scale, int causal, fa_dtype dtype, void *workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    if (D <= 0) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_BF16_OUT_F32) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t units = (int64_t)B * H;
+    if (units > INT32_MAX || (int64_t)N > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    const int64_t rows = units * N;
+    if (rows == 0) return FA_OK;
+    const void *ins[6] = {Q, K, V, O, dO, L};
+    void *outs[3] = {dQ, dK, dV};
+    for (const void *x : ins)
+        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARG;
+    for (const void *x : outs)
+        if (!x || !aligned16(x)) return FA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_workspace_size(B, H, N))
+        return FA_ERR_INVALID_ARG;
+    const size_t ni = (size_t)rows * D * in_bytes(dtype), no = (size_t)rows * D * out_bytes(dtype);
+    const size_t nl = (size_t)rows * sizeof(float), nw = (size_t)rows * sizeof(float);
+    const size_t in_sizes[6] = {ni, ni, ni, ni, ni, nl};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], no, ins[b], in_sizes[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], no, outs[b], no)) return FA_ERR_INVALID_ARG;
+        if (overlaps(outs[a], no, workspace, nw)) return FA_ERR_INVALID_ARG;
+    }
+    for (int b = 0; b < 6; ++b)
+        if (overlaps(workspace, nw, ins[b], in_sizes[b])) return FA_ERR_INVALID_ARG;
+
+    FaBwdProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.dout = dO;
+    p.lse = L;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.delta = static_cast<float *>(workspace);
+    p.units_bh = (int)units;
+    p.n = N;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.wl = -1;
+    p.wr = causal ? 0 : -1;
+    p.dtype = dtype;
+    p.stream = static_cast<cudaStream_t>(stream);
+    p.err = err_word();
+    if (!p.err) return FA_ERR_CUDA;
+    p.grid_ctas = g_opts.grid_ctas;
+    p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
+    fa_status st = fa_launch_bwd_delta(p);
+    if (st != FA_OK) return st;
+    const bool bf16 = dtype != FA_F32;
+    switch (g_opts.kernel) {
+        case FA_KERNEL_SIMT: return fa_launch_bwd_simt(p);
+        case FA_KERNEL_TC: return bf16 ? fa_launch_bwd_tc(p) : FA_ERR_UNSUPPORTED;
+        default:
+            if (!bf16) return fa_launch_bwd_simt(p);
+            st = fa_launch_bwd_tc(p);
+            return st == FA_ERR_UNSUPPORTED ? fa_launch_bwd_simt(p) : st;
+    }
+}
+
 fa_status fa_check_device_error(fa_stream_t stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t *err = err_word();

@@ -38,12 +38,37 @@ struct FaProblem {
     cudaStream_t stream;
 };
 
+// The backward pass (dense batch).  Row statistic delta = rowsum(dO * O)
+// lives in the caller's workspace.
+struct FaBwdProblem {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    float *delta;     // [B*H*N] float32 (workspace)
+    int units_bh;     // B*H
+    int n;            // N
+    int D;
+    float scale;
+    int causal;
+    int wl, wr;       // key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
+    int dtype;        // fa_dtype
+    uint32_t *err;
+    int grid_ctas;
+    uint64_t wait_limit_ns;
+    cudaStream_t stream;
+};
+
 // Record `e` as the calling thread's last CUDA failure (see
 // fa_last_cuda_error) and clear the runtime's sticky-free last error.
 // Returns FA_ERR_CUDA so launchers can `return fa_cuda_fail(e);`.
 fa_status fa_cuda_fail(cudaError_t e);
 
 fa_status fa_launch_simt(const FaProblem &p);
+// Backward pass: delta = rowsum(dO * O), then the FFMA or tensor-core
+// gradient kernels (each launcher runs the delta kernel itself).
+fa_status fa_launch_bwd_delta(const FaBwdProblem &p);
+fa_status fa_launch_bwd_simt(const FaBwdProblem &p);
+fa_status fa_launch_bwd_tc(const FaBwdProblem &p);
 fa_status fa_launch_tc(const FaProblem &p);
 
 // Split-key planning for the tensor-core kernel: the number of key-range

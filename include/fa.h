@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 library: the
+ * forward pass (fa_fwd and its variants) and its gradients (fa_bwd).
  *
  * The operation (for every batch b and head h, or every packed sequence s
  * and head h):
@@ -207,6 +208,50 @@ FA_API fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void
                                         void *O, float *L, int B, int H, int N, int D,
                                         float scale, int causal, fa_dtype dtype,
                                         int num_splits, fa_stream_t stream);
+
+/*
+ * fa_bwd -- gradients of the dense forward pass.  Given dO (the gradient of
+ * a loss with respect to O), the forward inputs Q, K, V and the forward
+ * outputs O and L, compute
+ *
+ *     P  = exp(scale * Q K^T - L)   (masked entries 0), recomputed tile by
+ *                                    tile, never stored ("FlashAttention --
+ *                                    for programmers, not researchers.",
+ *                                    STAGE 5: keep only the per-row
+ *                                    statistics, recompute the scores)
+ *     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+ *     dK = scale dS^T Q,  dQ = scale dS K
+ *                                   (the five contractions of the
+ *                                    "FlashAttention" docs page, section
+ *                                    "Application in Backward Pass
+ *                                    (5 MMAs)"; dS is the row-softmax
+ *                                    derivative)
+ *
+ *   Q, K, V, O, dO : [B, H, N, D] contiguous; bf16 for FA_BF16 and
+ *                    FA_BF16_OUT_F32, float32 for FA_F32.  O and L must be
+ *                    the forward pass's outputs for the same Q, K, V,
+ *                    scale and mask (O may be bf16-rounded).
+ *   L              : [B, H, N] float32
+ *   dQ, dK, dV     : [B, H, N, D] outputs: bf16 for FA_BF16, float32 for
+ *                    FA_BF16_OUT_F32 and FA_F32.  They must not overlap any
+ *                    input, each other or the workspace.
+ *   workspace      : DEVICE memory of at least fa_bwd_workspace_size(B, H,
+ *                    N) bytes, 16-byte aligned, owned by the caller; it
+ *                    holds rowsum(dO * O) per row.  Contents on entry are
+ *                    ignored.
+ *
+ * Deterministic: no atomics; dK/dV and dQ come from separate passes (dK and
+ * dV owned by key blocks, dQ by query blocks), each summing in a fixed order.
+ * Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a short or null workspace.
+ */
+FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O,
+                        const void *dO, const float *L, void *dQ, void *dK, void *dV, int B,
+                        int H, int N, int D, float scale, int causal, fa_dtype dtype,
+                        void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Workspace bytes fa_bwd needs: 4 * B * H * N rounded up to 256 (0 for an
+ * empty problem or negative sizes). */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N);
 
 /*
  * fa_check_device_error -- synchronise `stream`, then return (and clear)

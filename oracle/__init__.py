@@ -29,6 +29,8 @@ The oracle is written from the definition of attention, in float64 NumPy:
   (5 MMAs)", lists.
 * ``attention_bwd_recompute`` -- the same gradients by STAGE 5's route:
   P recomputed tile by tile from Q, K and the stored L.
+* ``attention_bwd_sampled`` -- chosen rows of dQ and keys of dK, dV of one
+  head, for checking full-size runs.
 
 Every function here is pinned by ``tests/test_oracle.py`` and
 ``tests/test_oracle_bwd.py`` against closed forms, brute force in pure
@@ -46,5 +48,6 @@ from .backward import (  # noqa: F401
     attention_bwd_recompute,
     attention_bwd_ref,
     attention_bwd_ref_varlen,
+    attention_bwd_sampled,
     forward_for_backward,
 )

@@ -154,3 +154,52 @@ def forward_for_backward(q, k, v, scale: float, causal: bool, window=None):
     stored inputs."""
     qf, kf, vf = _f64(q), _f64(k), _f64(v)
     return _attend(qf, kf, vf, float(scale), causal, np.arange(qf.shape[0]), window=window)
+
+
+def _visible_col(n: int, j: int, causal: bool, window) -> np.ndarray:
+    """Boolean [n]: rows i that see key j."""
+    i = np.arange(n)
+    keep = np.ones(n, dtype=bool)
+    if causal:
+        keep &= j <= i
+    if window is not None:
+        wl, wr = window
+        if wl >= 0:
+            keep &= j >= i - wl
+        if wr >= 0:
+            keep &= j <= i + wr
+    return keep
+
+
+def attention_bwd_sampled(q, k, v, do, scale: float, causal: bool, rows, keys, window=None):
+    """dQ at the query rows ``rows`` and dK, dV at the keys ``keys`` of ONE
+    head, without forming any (n, n) matrix: O and L of every row come from
+    the forward definition, then each requested row of dQ and column of dK,
+    dV is the definition above restricted to it (dQ_i = scale sum_j dS_ij K_j,
+    dK_j = scale sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i).
+
+    q, k: [n, d]; v, do: [n, dv].  Returns (dq [len(rows), d],
+    dk [len(keys), d], dv [len(keys), dv]) in float64.
+    """
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    n = qf.shape[0]
+    o, lse = _attend(qf, kf, vf, float(scale), causal, np.arange(n), window=window)
+    delta = np.sum(dof * o, axis=1)
+    rows, keys = np.asarray(rows, dtype=np.int64), np.asarray(keys, dtype=np.int64)
+    dq = np.zeros((len(rows), qf.shape[1]))
+    for t, i in enumerate(rows):
+        keep = _mask(n, np.array([i]), causal, window)[0]
+        with np.errstate(over="ignore", invalid="ignore"):
+            p = np.where(keep, np.exp(scale * (kf @ qf[i]) - lse[i]), 0.0)
+        ds = p * (vf @ dof[i] - delta[i])
+        dq[t] = scale * (ds @ kf)
+    dk = np.zeros((len(keys), kf.shape[1]))
+    dv = np.zeros((len(keys), vf.shape[1]))
+    for t, j in enumerate(keys):
+        keep = _visible_col(n, int(j), causal, window)
+        with np.errstate(over="ignore", invalid="ignore"):
+            p = np.where(keep, np.exp(scale * (qf @ kf[j]) - lse), 0.0)
+        ds = p * (dof @ vf[j] - delta)
+        dv[t] = p @ dof
+        dk[t] = scale * (ds @ qf)
+    return dq, dk, dv

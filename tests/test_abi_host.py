@@ -170,3 +170,51 @@ def test_splitkv_workspace_size(lib):
         fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 3)                # capped at ceil(N/128)
     assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1024, 96, 3) == 0      # unsupported D
     assert fa.fa_fwd_splitkv_workspace_size(0, 1, 1024, 128, 3) == 0
+
+
+# ------------------------------------------------------------ backward --
+def _bwd_ptrs():
+    return [A + i * STEP for i in range(10)]   # Q K V O dO L dQ dK dV workspace
+
+
+def test_bwd_workspace_size(lib):
+    assert fa.fa_bwd_workspace_size(2, 16, 4096) == 2 * 16 * 4096 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 3) == 256          # rounded up to 256
+    for B, H, N in [(0, 1, 16), (1, 0, 16), (1, 1, 0), (-1, 1, 16)]:
+        assert fa.fa_bwd_workspace_size(B, H, N) == 0
+
+
+def test_bwd_argument_checks(lib):
+    q, k, v, o, do, l, dq, dk, dv, ws = _bwd_ptrs()
+    nws = fa.fa_bwd_workspace_size(1, 1, 16)
+    bad, uns = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(*, B=1, H=1, N=16, D=64, scale=0.1, causal=0, dtype=fa.FA_BF16, p=None, w=ws,
+             nw=nws):
+        args = list(p or (q, k, v, o, do, l, dq, dk, dv))
+        return fa.fa_bwd(*args, B, H, N, D, scale, causal, dtype, w, nw, 0)
+
+    assert call(B=-1) == bad and call(H=-1) == bad and call(N=-4) == bad
+    assert call(D=0) == bad and call(D=96) == uns and call(D=256) == uns
+    assert call(scale=float("nan")) == bad and call(causal=2) == bad and call(dtype=9) == bad
+    # null or misaligned pointers, short or missing workspace
+    for i in range(9):
+        p = [q, k, v, o, do, l, dq, dk, dv]
+        p[i] = 0
+        assert call(p=p) == bad
+        p[i] = [q, k, v, o, do, l, dq, dk, dv][i] + 8
+        assert call(p=p) == bad
+    assert call(w=0) == bad and call(w=ws + 4) == bad and call(nw=nws - 4) == bad
+    # outputs overlapping inputs, each other or the workspace
+    assert call(p=[q, k, v, o, do, l, q + 64, dk, dv]) == bad
+    assert call(p=[q, k, v, o, do, l, dq, dq + 64, dv]) == bad
+    assert call(p=[q, k, v, o, do, l, dq, dk, l]) == bad
+    assert call(p=[q, k, v, o, do, l, dq, dk, ws]) == bad
+    assert call(w=do + 32) == bad
+    # empty problems are no-ops and touch nothing
+    for B, H, N in [(0, 1, 16), (1, 0, 16), (1, 1, 0)]:
+        assert fa.fa_bwd(0, 0, 0, 0, 0, 0, 0, 0, 0, B, H, N, 64, 0.1, 1, fa.FA_BF16, 0, 0,
+                         0) == fa.FA_OK
+    if not torch.cuda.is_available():   # valid arguments reach CUDA, which is absent
+        assert call() == fa.FA_ERR_CUDA
+        assert call(dtype=fa.FA_F32) == fa.FA_ERR_CUDA

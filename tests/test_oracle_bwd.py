@@ -253,3 +253,28 @@ def test_bwd_batched_leading_dims():
             ref = attention_bwd_ref(q[b, h], k[b, h], v[b, h], do[b, h], 0.5, True)
             for a, c in zip(got, ref):
                 assert np.array_equal(a[b, h], c)
+
+
+@pytest.mark.parametrize("pin", BWD_PINS, ids=lambda p: p.__name__)
+def test_bwd_sampled_pins(pin):
+    """Every row and key taken one at a time, in reversed order."""
+    from oracle import attention_bwd_sampled
+
+    def grad(q, k, v, do, s, c):
+        n = np.asarray(q).shape[0]
+        idx = np.arange(n)[::-1]
+        dq, dk, dv = attention_bwd_sampled(q, k, v, do, s, c, idx, idx)
+        return dq[::-1], dk[::-1], dv[::-1]
+    pin(grad)
+
+
+def test_bwd_sampled_band_matches_definition():
+    from oracle import attention_bwd_sampled
+    q, k, v, do = _case(16, 90, 8, 5)
+    for causal, window in ((False, (10, 3)), (True, None), (False, (-1, 7))):
+        ref = attention_bwd_ref(q, k, v, do, 0.5, causal, window=window)
+        rows, keys = [0, 1, 44, 89], [0, 30, 88, 89]
+        dq, dk, dv = attention_bwd_sampled(q, k, v, do, 0.5, causal, rows, keys, window=window)
+        assert np.max(np.abs(dq - ref[0][rows])) <= 1e-13
+        assert np.max(np.abs(dk - ref[1][keys])) <= 1e-13
+        assert np.max(np.abs(dv - ref[2][keys])) <= 1e-13

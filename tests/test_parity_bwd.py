@@ -1,0 +1,156 @@
+"""GPU parity of the backward pass (fa_bwd through the C ABI) against the
+float64 oracle on the same seeded inputs, element by element.
+
+The kernel is given the oracle's O and L, stored in the library's types
+(O in the input dtype, L float32), so these tests check the backward
+kernels alone.  The expected gradients come from the oracle's own
+definition on Q, K, V, dO.
+
+Tolerance: the pages state none for gradients.  The forward bounds are
+applied relative to each gradient tensor's scale: max abs error <=
+tol * max(1, max |ref|), with tol = 1e-4 for float32 and 1e-2 for bf16
+inputs (P and dS enter the tensor-core contractions as bf16, as P does in
+the forward pass), plus half a bf16 ulp of |ref| when the gradient is
+stored as bf16.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_24_gb300 as fa
+from exact_attention_24_gb300 import build as fa_build
+from exact_attention_24_gb300.workloads import Workload, make_inputs
+from helpers import half_ulp_bf16, to_f64
+from oracle import attention_bwd_ref, attention_bwd_sampled, attention_ref
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+GRAD_TOL = {fa.FA_F32: 1e-4, fa.FA_BF16_OUT_F32: 1e-2, fa.FA_BF16: 1e-2}
+BF16_CODES = (fa.FA_BF16_OUT_F32, fa.FA_BF16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa_build.build()
+    fa.load_library()
+    yield
+    fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+
+
+@pytest.fixture(params=["auto", "simt"])
+def kernel(request):
+    code = fa.FA_KERNEL_AUTO if request.param == "auto" else fa.FA_KERNEL_SIMT
+    assert fa.fa_set_options(code, 0, 0) == fa.FA_OK
+    yield request.param
+    fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+
+
+def _bwd_inputs(B, H, N, D, dtype, causal, seed, qk_mult=1.0):
+    """Seeded Q, K, V, dO (storage dtype) and the oracle's O, L for them."""
+    w = Workload("bwd", B, H, N, D, dtype, causal, seed, qk_mult)
+    q, k, v = make_inputs(w)
+    do = make_inputs(Workload("dO", B, H, N, D, dtype, causal, seed + 50_000))[0]
+    o, lse = attention_ref(q, k, v, w.scale, causal)
+    return w, q, k, v, do, torch.from_numpy(o).to(q.dtype), torch.from_numpy(lse).float()
+
+
+def run_bwd(q, k, v, o, do, lse, causal, code, scale):
+    B, H, N, D = q.shape
+    odt = torch.bfloat16 if code == fa.FA_BF16 else torch.float32
+    grads = [torch.full((B, H, N, D), float("nan"), dtype=odt, device=q.device) for _ in range(3)]
+    nbytes = fa.fa_bwd_workspace_size(B, H, N)
+    ws = torch.full((max(nbytes, 16) // 4,), float("nan"), dtype=torch.float32, device=q.device)
+    st = fa.fa_bwd(q, k, v, o, do, lse, *grads, B, H, N, D, scale, int(causal), code, ws, nbytes,
+                   None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    return grads
+
+
+def assert_grads(got, ref, code, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = np.asarray(g)
+        assert g.shape == r.shape, (what, name)
+        assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
+        bound = GRAD_TOL[code] * max(1.0, float(np.max(np.abs(r), initial=0.0)))
+        bound = bound + (half_ulp_bf16(r) if code == fa.FA_BF16 else 0.0)
+        excess = np.abs(g - r) - bound
+        i = np.unravel_index(np.argmax(excess), excess.shape)
+        assert excess[i] <= 0, (f"{what}: {name} err {abs(g[i] - r[i]):.3e} at "
+                                f"{tuple(int(x) for x in i)} (got {g[i]:.6f}, ref {r[i]:.6f})")
+
+
+SHAPES = [(1, 1, 1, 64), (1, 1, 3, 128), (1, 1, 127, 64), (1, 2, 129, 128), (1, 1, 257, 64),
+          (2, 2, 300, 128), (1, 1, 700, 64), (1, 3, 1000, 128)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_small_bf16(kernel, shape, causal):
+    B, H, N, D = shape
+    w, q, k, v, do, o, lse = _bwd_inputs(B, H, N, D, "bf16", causal, seed=3 * N + D)
+    ref = attention_bwd_ref(q, k, v, do, w.scale, causal)[:3]
+    dev = [x.to(DEV) for x in (q, k, v, o, do, lse)]
+    for code in BF16_CODES:
+        got = run_bwd(*dev, causal, code, w.scale)
+        assert_grads([to_f64(x) for x in got], ref, code, f"{kernel} {shape} c={causal} dt={code}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64), (1, 1, 5, 128), (2, 2, 300, 64),
+                                   (1, 2, 513, 128)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_small_f32(kernel, shape, causal):
+    B, H, N, D = shape
+    w, q, k, v, do, o, lse = _bwd_inputs(B, H, N, D, "f32", causal, seed=5 * N + D)
+    ref = attention_bwd_ref(q, k, v, do, w.scale, causal)[:3]
+    got = run_bwd(*[x.to(DEV) for x in (q, k, v, o, do, lse)], causal, fa.FA_F32, w.scale)
+    assert_grads([to_f64(x) for x in got], ref, fa.FA_F32, f"{kernel} {shape} c={causal}")
+
+
+def test_bwd_sharp_softmax(kernel):
+    """Q, K doubled (the sharp-softmax workload's recipe): P is nearly
+    one-hot, large entries of dS."""
+    w, q, k, v, do, o, lse = _bwd_inputs(1, 2, 640, 64, "bf16", True, seed=77, qk_mult=2.0)
+    ref = attention_bwd_ref(q, k, v, do, w.scale, True)[:3]
+    got = run_bwd(*[x.to(DEV) for x in (q, k, v, o, do, lse)], True, fa.FA_BF16_OUT_F32, w.scale)
+    assert_grads([to_f64(x) for x in got], ref, fa.FA_BF16_OUT_F32, f"{kernel} sharp")
+
+
+def test_bwd_deterministic(kernel):
+    """No atomics: two calls give bitwise the same gradients."""
+    w, q, k, v, do, o, lse = _bwd_inputs(2, 2, 1000, 128, "bf16", True, seed=3)
+    dev = [x.to(DEV) for x in (q, k, v, o, do, lse)]
+    a = run_bwd(*dev, True, fa.FA_BF16, w.scale)
+    b = run_bwd(*dev, True, fa.FA_BF16, w.scale)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_bwd_from_own_forward(kernel):
+    """The usual pairing: L and O from fa_fwd itself feed fa_bwd."""
+    w, q, k, v, do, _, _ = _bwd_inputs(1, 2, 900, 128, "bf16", True, seed=11)
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    O, L = fa.attention(qd, kd, vd, causal=True, scale=w.scale)
+    got = run_bwd(qd, kd, vd, O, dod, L, True, fa.FA_BF16_OUT_F32, w.scale)
+    ref = attention_bwd_ref(q, k, v, do, w.scale, True)[:3]
+    assert_grads([to_f64(x) for x in got], ref, fa.FA_BF16_OUT_F32, f"{kernel} own forward")
+
+
+@pytest.mark.parametrize("shape", [(2, 16, 4096, 128, True), (4, 8, 1024, 64, False)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bwd_full_size_sampled(shape):
+    """Benchmark-sized problems (the C3 and C2 shapes) in the default kernel
+    selection, checked on sampled rows of dQ and keys of dK, dV."""
+    B, H, N, D, causal = shape
+    w, q, k, v, do, o, lse = _bwd_inputs(B, H, N, D, "bf16", causal, seed=123)
+    got = run_bwd(*[x.to(DEV) for x in (q, k, v, o, do, lse)], causal, fa.FA_BF16, w.scale)
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.integers(0, N, 20)]))
+    for b, h in [(0, 0), (B - 1, H - 1)]:
+        ref = attention_bwd_sampled(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, causal, idx, idx)
+        mine = [to_f64(got[0][b, h, idx]), to_f64(got[1][b, h, idx]), to_f64(got[2][b, h, idx])]
+        assert_grads(mine, ref, fa.FA_BF16, f"full {shape} b={b} h={h}")
