@@ -1,7 +1,488 @@
 // Tensor-core (tcgen05) backward pass.
-#include "fa_internal.h"
+//
+// The gradients of "FlashAttention -- for programmers, not researchers.",
+// STAGE 5: the probabilities are recomputed tile by tile from Q, K and the
+// forward pass's L, P = exp(scale Q K^T - L), never stored.  The five
+// contractions of the "FlashAttention" docs page, section "Application in
+// Backward Pass (5 MMAs)", run in two kernels so that every output has one
+// owner and every sum a fixed order (no atomics):
+//
+//   dK/dV kernel, one 128-key block per CTA, K and V resident:
+//     S^T = K Q_i^T, dP^T = V dO_i^T           (128 x 128, lanes = keys)
+//     P^T = exp2(S^T c - L_i log2 e), dS^T = P^T (dP^T - delta_i)
+//     dV += P^T dO_i, dK += dS^T Q_i           (A operand from TMEM)
+//   dQ kernel, one 128-row query block per CTA, Q and dO resident:
+//     S = Q K_j^T, dP = dO V_j^T               (lanes = query rows)
+//     P, dS as above; dQ += dS K_j             (A operand from TMEM)
+//
+// Both are made of the forward pass's two MMA shapes (A B^T with both
+// operands K-major in shared memory; A from TMEM times an MN-major shared
+// operand).  The streamed operand pair (Q_i and dO_i, or K_j and V_j) flows
+// through a two-stage TMA ring.  Warps 0-3 turn S, dP into P, dS (one TMEM
+// lane, i.e. one key or one query row, per thread), warp 4 is the TMA
+// producer, warp 5 allocates TMEM and issues the MMAs.  Every wait is
+// bounded (the device watchdog of the forward kernel).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "device_common.cuh"
+#include "tc_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kT = kTcRows;          // 128 rows / keys per tile
+constexpr int kBwdThreads = 192;
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kStages = 2;           // streamed operand pairs in flight
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = kT * D * 2;
+    static constexpr int kRingOff = 2 * kTileBytes;                  // after the resident pair
+    static constexpr int kStatOff = kRingOff + 2 * kStages * kTileBytes;
+    static constexpr int kStatBytes = kStages * 2 * kT * 4;          // [stage][L, delta][128]
+    static constexpr int kBarOff = kStatOff + kStatBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;    // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(2 * kT + 2 * D <= (int)kTmemCols, "TMEM columns");
+};
+
+struct BwdTcParams {
+    const float *lse, *delta;
+    void *dq, *dk, *dv;
+    int n, nblk;
+    float scale, scale_log2;
+    int causal;
+    uint32_t *err;
+    uint64_t wait_limit_ns;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void store_row(float *dst, const float *x, float mul) {
+    float4 *d = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        d[i] = make_float4(x[4 * i] * mul, x[4 * i + 1] * mul, x[4 * i + 2] * mul, x[4 * i + 3] * mul);
+}
+__device__ __forceinline__ void store_row(__nv_bfloat16 *dst, const float *x, float mul) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = make_uint4(pack_bf16x2(x[8 * i] * mul, x[8 * i + 1] * mul),
+                          pack_bf16x2(x[8 * i + 2] * mul, x[8 * i + 3] * mul),
+                          pack_bf16x2(x[8 * i + 4] * mul, x[8 * i + 5] * mul),
+                          pack_bf16x2(x[8 * i + 6] * mul, x[8 * i + 7] * mul));
+}
+
+// TMA: one 128-row tile (all D columns) of a [units][n][D] bf16 tensor.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int row,
+                                          int unit) {
+#pragma unroll
+    for (int hf = 0; hf < BCfg<D>::kHalves; ++hf)
+        tma_load_3d(dst + hf * kTcAtomBytes, tm, bar, hf * 64, row, unit);
+}
+
+// Shared layout of both kernels' barriers: fixed-pair full, ring full/empty
+// per stage, S-and-dP ready, P/dS ready, accumulators final, drain.
+struct Bars {
+    uint32_t fix_full, ring_full, ring_empty, s_full, p_full, o_final, drain;
+    __device__ explicit Bars(uint32_t b)
+        : fix_full(b), ring_full(b + 8), ring_empty(b + 8 + 8 * kStages), s_full(b + 8 + 16 * kStages),
+          p_full(b + 16 + 16 * kStages), o_final(b + 24 + 16 * kStages), drain(b + 32 + 16 * kStages) {}
+};
+static_assert(40 + 16 * kStages + 16 <= 256, "barrier area");
+
+__device__ __forceinline__ void init_bars(const Bars &b) {
+    mbar_init(b.fix_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(b.ring_full + 8 * s, 1);
+        mbar_init(b.ring_empty + 8 * s, 1);
+    }
+    mbar_init(b.s_full, 1);
+    mbar_init(b.p_full, 4);
+    mbar_init(b.o_final, 1);
+    mbar_init(b.drain, 1);
+    fence_barrier_init();
+}
+
+// Producer: the resident pair (fixed rows), then `tiles` streamed pairs.
+template <int D>
+__device__ void produce(const Bars &b, uint32_t base, const CUtensorMap *tm_f0, const CUtensorMap *tm_f1,
+                        const CUtensorMap *tm_r0, const CUtensorMap *tm_r1, int fixed_row, int first_row,
+                        int tiles, int unit, const WaitCtx &wc, uint64_t lim) {
+    using C = BCfg<D>;
+    mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
+    load_tile<D>(base, tm_f0, b.fix_full, fixed_row, unit);
+    load_tile<D>(base + C::kTileBytes, tm_f1, b.fix_full, fixed_row, unit);
+    int t = 0;
+    for (; t < tiles; ++t) {
+        const int s = t % kStages, round = t / kStages;
+        if (round > 0 && !mbar_wait(b.ring_empty + 8 * s, (round - 1) & 1, wc, 0x41)) break;
+        const uint32_t dst = base + C::kRingOff + s * 2 * C::kTileBytes;
+        mbar_arrive_expect_tx(b.ring_full + 8 * s, 2 * C::kTileBytes);
+        load_tile<D>(dst, tm_r0, b.ring_full + 8 * s, first_row + t * kT, unit);
+        load_tile<D>(dst + C::kTileBytes, tm_r1, b.ring_full + 8 * s, first_row + t * kT, unit);
+    }
+    // Teardown: every copy issued lands before the CTA exits.
+    mbar_drain(b.fix_full, 0, lim);
+    for (int u = t > kStages ? t - kStages : 0; u < t; ++u)
+        mbar_drain(b.ring_full + 8 * (u % kStages), (u / kStages) & 1, lim);
+}
+
+// MMA warp: per streamed tile, S = F0 R0^T and dP = F1 R1^T (or the
+// transposed forms), then once P / dS are in TMEM, acc0 (+)= P R1 and
+// acc1 (+)= dS R_x with R_x the MN-major view of the streamed tile `acc1_src`
+// (0: R0, 1: R1) ... see the two callers.
+struct MmaPlan {
+    uint32_t t_s, t_dp, t_acc0, t_acc1;  // TMEM addresses
+    int acc0_b, acc1_b;                  // streamed tile feeding acc0 / acc1 (0 or 1)
+    bool two_acc;                        // dK/dV kernel: two accumulators
+};
+
+template <int D>
+__device__ void mma_role(const Bars &b, uint32_t base, const MmaPlan &m, int tiles, const WaitCtx &wc,
+                         uint64_t lim) {
+    using C = BCfg<D>;
+    constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
+    const uint64_t d_f0 = smem_desc(base, 16, 1024), d_f1 = d_f0 + kTileDesc;
+    const uint64_t d_ring_k = smem_desc(base + C::kRingOff, 16, 1024);          // K-major view
+    const uint64_t d_ring_mn = smem_desc(base + C::kRingOff, kTcAtomBytes, 1024);  // MN-major view
+    bool ok = warp_wait(b.fix_full, 0, wc, 0x50);
+    for (int t = 0; ok && t < tiles; ++t) {
+        const int s = t % kStages;
+        if (!warp_wait(b.ring_full + 8 * s, (t / kStages) & 1, wc, 0x51)) break;
+        tc_fence_after();
+        const uint64_t r0 = s * 2 * kTileDesc, r1 = r0 + kTileDesc;
+        if (elect_one()) {
+            issue_qk<D>(m.t_s, d_f0, d_ring_k + r0);
+            issue_qk<D>(m.t_dp, d_f1, d_ring_k + r1);
+            mma_commit(b.s_full);
+        }
+        __syncwarp();
+        if (!warp_wait(b.p_full, t & 1, wc, 0x52)) break;
+        tc_fence_after();
+        if (elect_one()) {
+            const uint32_t acc = t > 0 ? 1u : 0u;
+            if (m.two_acc) {
+                issue_pv<D>(m.t_acc0, m.t_s, d_ring_mn + (m.acc0_b ? r1 : r0), acc);    // dV += P^T dO
+                issue_pv<D>(m.t_acc1, m.t_dp, d_ring_mn + (m.acc1_b ? r1 : r0), acc);   // dK += dS^T Q
+            } else {
+                issue_pv<D>(m.t_acc0, m.t_s, d_ring_mn + (m.acc0_b ? r1 : r0), acc);    // dQ += dS K
+            }
+            mma_commit(b.ring_empty + 8 * s);
+        }
+        __syncwarp();
+    }
+    if (elect_one()) {
+        mma_commit(b.o_final);
+        mma_commit(b.drain);
+    }
+    __syncwarp();
+    mbar_drain(b.drain, 0, lim);
+}
+
+// ------------------------------------------------------------ dK, dV --
+template <int D, typename Tout>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdTcParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const Bars b(base + C::kBarOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
+    float *stat = reinterpret_cast<float *>(gbase + C::kStatOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int unit = blockIdx.x / p.nblk, jb = blockIdx.x % p.nblk;  // lowest key block first
+    const int j0 = jb * kT;
+    const int i_first = p.causal ? j0 : 0;
+    const int tiles = (p.n - i_first + kT - 1) / kT;
+
+    if (warp == kProdWarp && lane == 0) {
+        init_bars(b);
+        *abort_flag = 0;
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
+    const float *L = p.lse + (int64_t)unit * p.n;
+    const float *Dl = p.delta + (int64_t)unit * p.n;
+
+    if (warp == kProdWarp) {
+        if (lane == 0)
+            produce<D>(b, base, &tm_k, &tm_v, &tm_q, &tm_do, j0, i_first, tiles, unit, wc, p.wait_limit_ns);
+    } else if (warp == kMmaWarp) {
+        // S^T = K Q^T, dP^T = V dO^T; dV += P^T dO (dO: streamed tile 1),
+        // dK += dS^T Q (Q: streamed tile 0).
+        const MmaPlan m{tmem, tmem + kT, tmem + 2 * kT, tmem + 2 * kT + D, 1, 0, true};
+        mma_role<D>(b, base, m, tiles, wc, p.wait_limit_ns);
+    } else {
+        // ---------------------------------------------- P^T and dS^T
+        const int r = warp * 32 + lane;           // key within the block (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_s = tmem + lane_off, t_dp = t_s + kT;
+        const uint32_t t_dv = t_s + 2 * kT, t_dk = t_dv + D;
+        const float c = p.scale_log2;
+        // this thread stages the row statistics of query r of each tile,
+        // loaded one tile ahead
+        int iq = i_first + r;
+        float nl = iq < p.n ? L[iq] * kLog2e : INFINITY, nd = iq < p.n ? Dl[iq] : 0.f;
+        bool ok = true;
+        for (int t = 0; t < tiles; ++t) {
+            float *sl = stat + (t % kStages) * 2 * kT, *sd = sl + kT;
+            sl[r] = nl;
+            sd[r] = nd;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            iq += kT;
+            if (t + 1 < tiles) {
+                nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
+                nd = iq < p.n ? Dl[iq] : 0.f;
+            }
+            if (!warp_wait(b.s_full, t & 1, wc, 0x60)) { ok = false; break; }
+            tc_fence_after();
+            const bool diag = p.causal && t == 0;  // query q sees key r iff q >= r
+#pragma unroll
+            for (int cc = 0; cc < kT / 32; ++cc) {
+                float sv[32], dpv[32];
+                tmem_ld32(t_s + cc * 32, sv);
+                tmem_ld32(t_dp + cc * 32, dpv);
+                tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    const int qi = cc * 32 + x;
+                    float p0 = ex2_approx(fmaf(sv[x], c, -sl[qi]));
+                    float p1 = ex2_approx(fmaf(sv[x + 1], c, -sl[qi + 1]));
+                    if (diag) {
+                        if (qi < r) p0 = 0.f;
+                        if (qi + 1 < r) p1 = 0.f;
+                    }
+                    pk[x / 2] = pack_bf16x2(p0, p1);
+                    dk[x / 2] = pack_bf16x2(p0 * (dpv[x] - sd[qi]), p1 * (dpv[x + 1] - sd[qi + 1]));
+                }
+                tmem_st16(t_s + cc * 16, pk);    // P^T over S^T columns already read
+                tmem_st16(t_dp + cc * 16, dk);   // dS^T over dP^T columns already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.p_full);
+        }
+        if (ok && warp_wait(b.o_final, 0, wc, 0x61)) {
+            tc_fence_after();
+            const int key = j0 + r;
+            Tout *dV = static_cast<Tout *>(p.dv) + ((int64_t)unit * p.n + key) * D;
+            Tout *dK = static_cast<Tout *>(p.dk) + ((int64_t)unit * p.n + key) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float x[32];
+                tmem_ld32(t_dv + cc * 32, x);
+                tmem_wait_ld();
+                if (key < p.n) store_row(dV + cc * 32, x, 1.f);
+                tmem_ld32(t_dk + cc * 32, x);
+                tmem_wait_ld();
+                if (key < p.n) store_row(dK + cc * 32, x, p.scale);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- dQ --
+template <int D, typename Tout>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdTcParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const Bars b(base + C::kBarOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int unit = blockIdx.x / p.nblk;
+    const int ib = p.nblk - 1 - blockIdx.x % p.nblk;  // highest query block first
+    const int i0 = ib * kT;
+    const int key_tiles = (p.n + kT - 1) / kT;
+    const int tiles = p.causal ? min(ib + 1, key_tiles) : key_tiles;
+
+    if (warp == kProdWarp && lane == 0) {
+        init_bars(b);
+        *abort_flag = 0;
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
+
+    if (warp == kProdWarp) {
+        if (lane == 0)
+            produce<D>(b, base, &tm_q, &tm_do, &tm_k, &tm_v, i0, 0, tiles, unit, wc, p.wait_limit_ns);
+    } else if (warp == kMmaWarp) {
+        // S = Q K^T, dP = dO V^T; dQ += dS K (K: streamed tile 0).  dS is
+        // written over S's columns, so the plan's "P" operand is dS here.
+        const MmaPlan m{tmem, tmem + kT, tmem + 2 * kT, 0, 0, 0, false};
+        mma_role<D>(b, base, m, tiles, wc, p.wait_limit_ns);
+    } else {
+        // ------------------------------------------------------- dS
+        const int r = warp * 32 + lane;           // query row within the block (TMEM lane)
+        const int row = i0 + r;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_s = tmem + lane_off, t_dp = t_s + kT, t_dq = t_s + 2 * kT;
+        const float c = p.scale_log2;
+        const float lrow = row < p.n ? p.lse[(int64_t)unit * p.n + row] * kLog2e : INFINITY;
+        const float drow = row < p.n ? p.delta[(int64_t)unit * p.n + row] : 0.f;
+        bool ok = true;
+        for (int t = 0; t < tiles; ++t) {
+            if (!warp_wait(b.s_full, t & 1, wc, 0x70)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = t * kT;
+            // keys past the causal diagonal or past the end are masked
+            const int lim = p.causal ? min(row + 1, p.n) : p.n;
+            const bool need_mask = key0 + kT > lim;
+#pragma unroll
+            for (int cc = 0; cc < kT / 32; ++cc) {
+                float sv[32], dpv[32];
+                tmem_ld32(t_s + cc * 32, sv);
+                tmem_ld32(t_dp + cc * 32, dpv);
+                tmem_wait_ld();
+                uint32_t dk[16];
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    float p0 = ex2_approx(fmaf(sv[x], c, -lrow));
+                    float p1 = ex2_approx(fmaf(sv[x + 1], c, -lrow));
+                    if (need_mask) {
+                        const int key = key0 + cc * 32 + x;
+                        if (key >= lim) p0 = 0.f;
+                        if (key + 1 >= lim) p1 = 0.f;
+                    }
+                    dk[x / 2] = pack_bf16x2(p0 * (dpv[x] - drow), p1 * (dpv[x + 1] - drow));
+                }
+                tmem_st16(t_s + cc * 16, dk);    // dS over S columns already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.p_full);
+        }
+        if (ok && warp_wait(b.o_final, 0, wc, 0x71)) {
+            tc_fence_after();
+            Tout *dQ = static_cast<Tout *>(p.dq) + ((int64_t)unit * p.n + row) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float x[32];
+                tmem_ld32(t_dq + cc * 32, x);
+                tmem_wait_ld();
+                if (row < p.n) store_row(dQ + cc * 32, x, p.scale);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename K>
+fa_status prepare(K kernel, int smem) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    if (a.maxThreadsPerBlock < kBwdThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
+}
+
+template <int D, typename Tout>
+fa_status launch(const FaBwdProblem &p) {
+    using C = BCfg<D>;
+    CUtensorMap tq, tk, tv, tdo;
+    const uint64_t n = (uint64_t)p.n, units = (uint64_t)p.units_bh;
+    const uint64_t rs = (uint64_t)D * 2, hs = n * D * 2;
+    if (!make_map(&tq, p.q, D, n, units, rs, hs, kT, 1) || !make_map(&tk, p.k, D, n, units, rs, hs, kT, 1) ||
+        !make_map(&tv, p.v, D, n, units, rs, hs, kT, 1) || !make_map(&tdo, p.dout, D, n, units, rs, hs, kT, 1))
+        return FA_ERR_CUDA;
+    BwdTcParams k;
+    k.lse = p.lse;
+    k.delta = p.delta;
+    k.dq = p.dq;
+    k.dk = p.dk;
+    k.dv = p.dv;
+    k.n = p.n;
+    k.nblk = (p.n + kT - 1) / kT;
+    k.scale = p.scale;
+    k.scale_log2 = p.scale * kLog2e;
+    k.causal = p.causal;
+    k.err = p.err;
+    k.wait_limit_ns = p.wait_limit_ns;
+    const long long grid = (long long)k.nblk * p.units_bh;
+    if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    static bool ready = false;  // per instantiation
+    if (!ready) {
+        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout>, C::kSmemBytes);
+        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout>, C::kSmemBytes);
+        if (st != FA_OK) return st;
+        ready = true;
+    }
+    bwd_dkdv_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, C::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, C::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
+}
+
+}  // namespace
+}  // namespace fa
 
 fa_status fa_launch_bwd_tc(const FaBwdProblem &p) {
-    (void)p;
-    return FA_ERR_UNSUPPORTED;
+    if (p.dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+    if (p.wl >= 0 || (p.wr >= 0 && !(p.causal && p.wr == 0))) return FA_ERR_UNSUPPORTED;
+    if ((int64_t)p.units_bh * p.n == 0) return FA_OK;
+    const bool f32 = p.dtype == FA_BF16_OUT_F32;
+    if (p.D == 64) return f32 ? fa::launch<64, float>(p) : fa::launch<64, __nv_bfloat16>(p);
+    return f32 ? fa::launch<128, float>(p) : fa::launch<128, __nv_bfloat16>(p);
 }

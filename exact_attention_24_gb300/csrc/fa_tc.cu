@@ -42,6 +42,7 @@
 #include <math.h>
 
 #include "device_common.cuh"
+#include "tc_common.cuh"
 
 namespace fa {
 namespace {
@@ -287,70 +288,6 @@ __device__ __forceinline__ bool decode_item(const TcParams &p, const Sched &sc, 
         item_ranges<WIN>(p, it);
     }
     return it.nkv > 0;
-}
-
-// Bounded wait by every lane of a warp, with a warp-uniform result (a lane
-// that gave up makes the whole warp give up, so control flow never diverges
-// around elect.sync / __syncwarp).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w,
-                                          uint32_t site) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
-}
-
-// Wait (whole warp) until ring load number `li` has landed in its slot.
-__device__ __forceinline__ bool ring_wait(uint32_t bar_full, uint32_t li, uint32_t slots, const WaitCtx &w,
-                                          uint32_t site) {
-    return warp_wait(bar_full + 8 * (li % slots), (li / slots) & 1, w, site);
-}
-
-// ------------------------------------------------ UMMA descriptor helpers --
-// Shared-memory matrix descriptor (tcgen05): start address, leading- and
-// stride-dimension byte offsets (>> 4), fixed version bits 46-47 = 1,
-// swizzle mode 2 (128-byte swizzle) in bits 61-63.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
-           ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9, 10-12 = 1), B transposed flag (bit 16: 1 = MN-major), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// S (TMEM, 128 x 128 fp32) = Q (smem, 128 x D) * K^T (smem, 128 x D): both
-// operands K-major with 128-byte swizzle; D/16 MMAs of K = 16.  Within a
-// 64-element swizzle atom the K offset is a plain byte offset (32 B per
-// step); the second half of D=128 is the next 16 KB box.  `dq`, `dk` are the
-// descriptors of the tiles' first byte; the address field sits in the low
-// bits, so an offset is added to the descriptor directly (in 16-byte units,
-// never carrying out of the 14-bit field: shared memory is below 256 KB).
-// The issue sequence is straight-line: the single issuing thread is the
-// tensor core's only feeder, so every cycle spent here is tensor idle time.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, 0);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32) >> 4);
-        mma_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
-    }
-}
-
-// O (TMEM, 128 x D fp32) (+)= P (TMEM, 128 x 128 bf16) * V (smem, 128 x D):
-// V is MN-major (D contiguous) with 128-byte swizzle: 8-key groups are
-// 1024 B apart (SBO), the two 64-column halves of D=128 are 16 KB apart
-// (LBO).  Each MMA consumes 16 keys: 8 TMEM columns of P, 2048 B of V.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint64_t dv,
-                                         uint32_t accumulate) {
-    constexpr uint32_t idesc = idesc_bf16(BM, D, 1);
-    mma_ts(d_tmem, a_tmem, dv, idesc, accumulate);
-#pragma unroll
-    for (int kk = 1; kk < BN / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc, 1u);
 }
 
 // --------------------------------------------------------------- kernel --
@@ -912,56 +849,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------ host side --
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                                               cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
-            fa_cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
-            return nullptr;
-        }
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// 3-D map over a bf16 tensor: dims {D, d1, d2} with byte strides {s1, s2};
-// box {64, b1, b2}; 128-byte swizzle; out-of-range elements read as zero.
-bool make_map(CUtensorMap *m, const void *ptr, int D, uint64_t d1, uint64_t d2, uint64_t s1,
-              uint64_t s2, uint32_t b1, uint32_t b2) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, d1, d2};
-    cuuint64_t strides[2] = {s1, s2};
-    cuuint32_t box[3] = {64, b1, b2};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        fa_cuda_fail(cudaErrorInvalidValue);
-        return false;
-    }
-    return true;
-}
-
-int num_sms() {
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            fa_cuda_fail(e);
-            sms = 0;
-        }
-    }
-    return sms;
-}
-
 // Workspace layout of split-key mode: partial O (fp32) then partial L.
 constexpr size_t kWsAlign = 256;
 inline size_t ws_o_bytes(int S, int units, int n, int D) {
