@@ -6,6 +6,11 @@ B=2, H=16, N=4096, D=128, bf16, causal (the N >= 4096, D = 128 workload on
 which the tensor-peak target is set).  FLOPs = 4 B H N^2 D / 2 (causal).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME | --shape B,H,N,D[,causal]] [--splits S] [--bwd]
+
+``--bwd`` times the backward pass (fa_bwd: the row statistic and the dK/dV
+and dQ kernels) on the same workload instead; its FLOPs are the five
+contractions, 2.5x the forward count.
 
 Prints ONE JSON line (rank 0).  Inputs are resident in HBM before the timed
 region; they rotate over enough copies that the bytes touched between two
@@ -360,6 +365,221 @@ def bench_ours(args, w, rank, world, local):
     return rec
 
 
+# -------------------------------------------------------------- backward --
+METRIC_BWD = "attention bwd TFLOP/s (bf16, five-matmul count) and % of GB300 BF16 peak"
+
+
+def bwd_flops(w) -> float:
+    """The five contractions S, dP, dV, dK, dQ at 2 n^2 d each (halved
+    under the causal mask): 2.5x the forward count.  The recomputation of S
+    and dP that the two-kernel split repeats is not counted."""
+    return 2.5 * w.flops()
+
+
+def bench_bwd(args, w, rank, world, local):
+    import torch
+    import exact_attention_24_gb300 as fa
+    from exact_attention_24_gb300.build import build
+    from exact_attention_24_gb300.workloads import make_inputs
+
+    if w.varlen or w.window:
+        raise SystemExit("--bwd covers dense causal or full attention")
+    build()
+    fa.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    wr = dataclasses.replace(w, seed=rank_seed(w.seed, rank))
+    q, k, v = make_inputs(wr)
+    do = make_inputs(dataclasses.replace(wr, seed=wr.seed + 50_000))[0]
+    code = fa.FA_BF16
+    shape = q.shape
+    tensor_b = q.numel() * 2
+    l_b = q.numel() // w.D * 4
+    per_copy = 5 * tensor_b + l_b + 3 * tensor_b
+    copies = max(2, math.ceil(2 * L2_BYTES / per_copy) + 1)
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.N)
+    with torch.cuda.stream(stream):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        bufs = []
+        for _ in range(copies):
+            qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+            O, L = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, stream=stream)
+            grads = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+            bufs.append((qd, kd, vd, O, dod, L, *grads))
+    torch.cuda.synchronize(dev)
+
+    def call(b):
+        st = fa.fa_bwd(*b, w.B, w.H, w.N, w.D, w.scale, int(w.causal), code, ws, ws_bytes, stream)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd")
+
+    for i in range(args.warmup):
+        call(bufs[i % copies])
+    st = fa.fa_check_device_error(stream)
+    if st != fa.FA_OK:
+        raise fa.FaError(st, "warm-up")
+    sampler = ClockSampler(smi_gpu_id(local))
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(bufs[i % copies])
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark()
+    barrier(world)
+    sampler.stop()
+    st = fa.fa_check_device_error(stream)
+    if st != fa.FA_OK:
+        raise fa.FaError(st, "timed region")
+    ms_local = ev0.elapsed_time(ev1)
+    ms = reduce_max(ms_local, world, device=dev)
+    flops = bwd_flops(w)
+    value = world * flops * args.steps / (ms * 1e-3) / 1e12
+    achieved = flops / (ms_local / args.steps * 1e-3) / 1e12
+
+    # e2e: inputs (Q, K, V, O, dO, L) from pinned host memory, gradients back
+    e2e_steps = max(3, min(args.steps, 20))
+    O0, L0 = bufs[0][3].cpu(), bufs[0][5].cpu()
+    hosts = [x.pin_memory() for x in (q, k, v, O0, do, L0)]
+    outs = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    b0 = bufs[0]
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dst, src in zip(b0[:6], hosts):
+                dst.copy_(src, non_blocking=True)
+            call(b0)
+            for dst, src in zip(outs, b0[6:]):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device=dev)
+    barrier(world)
+    peak, _, peak_kind = load_peaks()
+    return {
+        "metric": METRIC_BWD,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "pass": "backward", "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
+                   "flops_per_step": flops,
+                   "l2": f"inputs rotated over {copies} resident copies "
+                         f"({copies * per_copy / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
+                     "traffic": load_traffic("fa_bwd", w.name)},
+        "e2e": {"value": round(world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": 5 * tensor_b + l_b, "d2h_bytes_per_step": 3 * tensor_b,
+                "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+
+def _bwd_oracle_sample(w, views, dos, it, count, seed):
+    """Random dQ rows and dK/dV keys of one head and their five-matmul FLOPs
+    (2 d per visible pair for each contraction a row or key touches)."""
+    import numpy as np
+    from oracle import attention_bwd_sampled
+    h = it % len(views)
+    q, k, v = views[h]
+    n = q.shape[0]
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(n, size=min(count, n), replace=False))
+    keys = np.sort(rng.choice(n, size=min(count, n), replace=False))
+    vis_r = w.visible_keys(rows, n)
+    vis_k = (n - keys) if w.causal else np.full(keys.shape, n)   # rows that see each key
+    fl = float(np.sum(3 * 2 * vis_r * w.D) + np.sum(4 * 2 * vis_k * w.D))
+    t0 = time.perf_counter()
+    attention_bwd_sampled(q, k, v, dos[h], w.scale, w.causal, rows, keys)
+    return fl, time.perf_counter() - t0, len(rows) + len(keys)
+
+
+def _bwd_views(w):
+    from exact_attention_24_gb300.workloads import make_inputs
+    q, k, v = make_inputs(w)
+    do = make_inputs(dataclasses.replace(w, seed=w.seed + 50_000))[0]
+    qf, kf, vf, dof = (x.double().numpy() for x in (q, k, v, do))
+    views = head_views(w, qf, kf, vf)
+    dos = [dof[b, h] for b in range(w.B) for h in range(w.H)]
+    return views, dos
+
+
+def cpu_baseline_bwd(w, seconds: float):
+    views, dos = _bwd_views(w)
+    done, t_total, outs, it = 0.0, 0.0, 0, 0
+    while t_total < seconds:
+        fl, dt, c = _bwd_oracle_sample(w, views, dos, it, 32, it)
+        done += fl
+        t_total += dt
+        outs += c
+        it += 1
+    return {"value": done / t_total / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{outs} gradient rows and keys ({it} heads x 32 random dQ rows and 32 random "
+                      f"dK/dV keys, each head's forward recomputed) of {w.name}, float64 NumPy, "
+                      f"{t_total:.1f} s"}
+
+
+def bench_reference_bwd(args, w, rank, world):
+    """The backward oracle as it stands, on bounded samples sized so that
+    warm-up + steps take about 90 s."""
+    if rank != 0:
+        return None
+    views, dos = _bwd_views(w)
+    _, dt, c = _bwd_oracle_sample(w, views, dos, 0, 8, 0)
+    per_head = max(dt, 1e-4)
+    heads = max(1, int(90.0 / max(1, args.steps + args.warmup) / per_head))
+    for i in range(args.warmup):
+        _bwd_oracle_sample(w, views, dos, 1000 + i, 8, 1000 + i)
+    fl_total, t_total = 0.0, 0.0
+    for i in range(args.steps):
+        for h in range(heads):
+            fl, dt, _ = _bwd_oracle_sample(w, views, dos, i * heads + h, 8, i * heads + h)
+            fl_total += fl
+            t_total += dt
+    value = fl_total / t_total / 1e12
+    sample = (f"{heads} head(s) per step, 8 random dQ rows and 8 random dK/dV keys each "
+              f"(each head's forward recomputed), {args.steps} steps, of {w.name}; "
+              f"float64 NumPy backward oracle")
+    return {
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "pass": "backward", "B": w.B, "H": w.H, "N": w.N,
+                   "D": w.D, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # -------------------------------------------------------------- IO model --
 def io_model_bytes(w, br: int, bc: int) -> int:
     """HBM bytes of the tiled loop under the byte-counting rule of
@@ -502,6 +722,8 @@ def main(argv=None):
                     help="seconds of oracle time for cpu_baseline (0 = leave it out)")
     ap.add_argument("--splits", type=int, default=None,
                     help="time fa_fwd_splitkv with this many key splits (0 = automatic)")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass (fa_bwd) instead of the forward pass")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,D[,causal] instead of a named workload (bf16, seed 8)")
     args = ap.parse_args(argv)
@@ -522,18 +744,18 @@ def main(argv=None):
         world = max(world, 1)
 
     if args.impl == "reference":
-        rec = bench_reference(args, w, rank, world)
+        rec = (bench_reference_bwd if args.bwd else bench_reference)(args, w, rank, world)
         if rec is not None:
             print(json.dumps(rec), flush=True)
         return 0
 
     import torch
     init_dist(world, "nccl" if torch.cuda.is_available() else "gloo")
-    rec = bench_ours(args, w, rank, world, local)
+    rec = (bench_bwd if args.bwd else bench_ours)(args, w, rank, world, local)
     if rank == 0:
         if world == 1:
-            rec["cpu_baseline"] = (cpu_baseline(w, args.cpu_seconds)
-                                   if args.cpu_seconds > 0 else None)
+            base = cpu_baseline_bwd if args.bwd else cpu_baseline
+            rec["cpu_baseline"] = base(w, args.cpu_seconds) if args.cpu_seconds > 0 else None
         print(json.dumps(rec), flush=True)
     if world > 1:
         import torch.distributed as dist
