@@ -90,8 +90,8 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, u
         tma_load_3d(dst + hf * kTcAtomBytes, tm, bar, hf * 64, row, unit);
 }
 
-// Shared layout of both kernels' barriers: fixed-pair full, ring full/empty
-// per stage, S-and-dP ready, P/dS ready, accumulators final, drain.
+// Barriers of the dQ kernel: fixed-pair full, ring full/empty per stage,
+// S-and-dP ready, dS ready, accumulator final, drain.
 struct Bars {
     uint32_t fix_full, ring_full, ring_empty, s_full, p_full, o_final, drain;
     __device__ explicit Bars(uint32_t b)
@@ -190,17 +190,78 @@ __device__ void mma_role(const Bars &b, uint32_t base, const MmaPlan &m, int til
 }
 
 // ------------------------------------------------------------ dK, dV --
+// The streamed operands arrive as 64-row halves of a query tile (Q_x and
+// dO_x of tile t, x = 0, 1) through a ring of kSlots half-tile slots, and
+// each half has its own TMEM buffers S^T_x, dP^T_x (64 columns each).  While
+// the softmax warps turn one half into P^T, dS^T, the MMA warp accumulates
+// the other half and computes its next S^T, dP^T:
+//   for half u = 2t + x:  wait P_x(u); dV += P^T_x dO_x; dK += dS^T_x Q_x;
+//                         release slot u; S^T_x(u + 2) = K Q^T, dP^T_x(u + 2) = V dO^T
+// (a buffer is overwritten only after the accumulating MMAs that read it:
+// one issuing thread, executed in order).  The ring holds 2.5 tiles, so a
+// half-tile's load is issued two halves before its first MMA.
+template <int D>
+struct DkCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = kT * D * 2;       // K or V (128 rows)
+    static constexpr int kHalfBytes = 64 * D * 2;       // Q_x or dO_x (64 rows)
+    static constexpr int kHalfAtom = 64 * 128;          // one 64-element-wide box of 64 rows
+    static constexpr int kSlots = D == 128 ? 5 : 10;
+    static constexpr int kSlotBytes = 2 * kHalfBytes;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kStatOff = kRingOff + kSlots * kSlotBytes;
+    static constexpr int kStatBytes = 2 * 2 * 64 * 4;   // [half parity][L, delta][64]
+    static constexpr int kBarOff = kStatOff + kStatBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(8 * (1 + 2 * kSlots + 6) + 16 <= kBarBytes, "barrier area");
+};
+
+struct DkBars {
+    uint32_t fix_full, ring_full, ring_empty, s_full, p_full, o_final, drain;
+    __device__ DkBars(uint32_t b, int slots)
+        : fix_full(b), ring_full(b + 8), ring_empty(b + 8 + 8 * slots), s_full(b + 8 + 16 * slots),
+          p_full(b + 24 + 16 * slots), o_final(b + 40 + 16 * slots), drain(b + 48 + 16 * slots) {}
+};
+
+// S^T_x (TMEM, 128 keys x 64 queries fp32) = K (smem, 128 x D) * Q_x^T
+// (smem, 64 x D): both K-major; K's 64-element boxes are 16 KB apart, a
+// half-tile's 8 KB.
+template <int D>
+__device__ __forceinline__ void issue_st_half(uint32_t d_tmem, uint64_t da, uint64_t db) {
+    constexpr uint32_t idesc = idesc_bf16(kTcRows, 64, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t oa = (uint64_t)(((kk / 4) * kTcAtomBytes + (kk % 4) * 32) >> 4);
+        const uint64_t ob = (uint64_t)(((kk / 4) * DkCfg<D>::kHalfAtom + (kk % 4) * 32) >> 4);
+        mma_ss(d_tmem, da + oa, db + ob, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// acc (TMEM, 128 x D fp32) (+)= A (TMEM, 128 x 64 bf16) * B_x with B_x a
+// half-tile viewed MN-major (64 x D; boxes 8 KB apart): 4 MMAs of 16 rows.
+template <int D>
+__device__ __forceinline__ void issue_acc_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
+                                               uint32_t accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(kTcRows, D, 1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, db + (uint64_t)((kk * 2048) >> 4), idesc,
+               (kk > 0 || accumulate) ? 1u : 0u);
+}
+
 template <int D, typename Tout>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdTcParams p) {
-    using C = BCfg<D>;
+    using C = DkCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const Bars b(base + C::kBarOff);
+    const DkBars b(base + C::kBarOff, C::kSlots);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
     float *stat = reinterpret_cast<float *>(gbase + C::kStatOff);
@@ -209,10 +270,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int unit = blockIdx.x / p.nblk, jb = blockIdx.x % p.nblk;  // lowest key block first
     const int j0 = jb * kT;
     const int i_first = p.causal ? j0 : 0;
-    const int tiles = (p.n - i_first + kT - 1) / kT;
+    const int halves = 2 * ((p.n - i_first + kT - 1) / kT);
 
     if (warp == kProdWarp && lane == 0) {
-        init_bars(b);
+        mbar_init(b.fix_full, 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(b.ring_full + 8 * i, 1);
+            mbar_init(b.ring_empty + 8 * i, 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b.s_full + 8 * x, 1);
+            mbar_init(b.p_full + 8 * x, 4);
+        }
+        mbar_init(b.o_final, 1);
+        mbar_init(b.drain, 1);
+        fence_barrier_init();
         *abort_flag = 0;
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -228,68 +300,157 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
-    const float *L = p.lse + (int64_t)unit * p.n;
-    const float *Dl = p.delta + (int64_t)unit * p.n;
+    const uint32_t ring = base + C::kRingOff;
 
     if (warp == kProdWarp) {
-        if (lane == 0)
-            produce<D>(b, base, &tm_k, &tm_v, &tm_q, &tm_do, j0, i_first, tiles, unit, wc, p.wait_limit_ns);
+        // ---------------------------------------------------- producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
+            load_tile<D>(base, &tm_k, b.fix_full, j0, unit);
+            load_tile<D>(base + C::kTileBytes, &tm_v, b.fix_full, j0, unit);
+            int u = 0;
+            for (; u < halves; ++u) {
+                const int slot = u % C::kSlots, round = u / C::kSlots;
+                if (round > 0 && !mbar_wait(b.ring_empty + 8 * slot, (round - 1) & 1, wc, 0x41)) break;
+                const uint32_t dst = ring + slot * C::kSlotBytes, fb = b.ring_full + 8 * slot;
+                mbar_arrive_expect_tx(fb, C::kSlotBytes);
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    tma_load_3d(dst + hf * C::kHalfAtom, &tm_q, fb, hf * 64, i_first + 64 * u, unit);
+                    tma_load_3d(dst + C::kHalfBytes + hf * C::kHalfAtom, &tm_do, fb, hf * 64,
+                                i_first + 64 * u, unit);
+                }
+            }
+            const uint64_t lim = p.wait_limit_ns;
+            mbar_drain(b.fix_full, 0, lim);
+            for (int v = u > C::kSlots ? u - C::kSlots : 0; v < u; ++v)
+                mbar_drain(b.ring_full + 8 * (v % C::kSlots), (v / C::kSlots) & 1, lim);
+        }
     } else if (warp == kMmaWarp) {
-        // S^T = K Q^T, dP^T = V dO^T; dV += P^T dO (dO: streamed tile 1),
-        // dK += dS^T Q (Q: streamed tile 0).
-        const MmaPlan m{tmem, tmem + kT, tmem + 2 * kT, tmem + 2 * kT + D, 1, 0, true};
-        mma_role<D>(b, base, m, tiles, wc, p.wait_limit_ns);
+        // --------------------------------------------------------- MMA
+        constexpr uint64_t kTileDesc = C::kTileBytes >> 4, kSlotDesc = C::kSlotBytes >> 4;
+        constexpr uint64_t kHalfDesc = C::kHalfBytes >> 4;
+        const uint64_t d_k = smem_desc(base, 16, 1024), d_v = d_k + kTileDesc;
+        const uint64_t d_ring_k = smem_desc(ring, 16, 1024);                 // K-major view
+        const uint64_t d_ring_mn = smem_desc(ring, C::kHalfAtom, 1024);      // MN-major view
+        const uint32_t t_dv = tmem + 2 * kT, t_dk = t_dv + D;
+        bool ok = warp_wait(b.fix_full, 0, wc, 0x50);
+        // S^T_x, dP^T_x of half u (buffer x = u & 1) from its ring slot
+        for (int u = 0; ok && u < 2 && u < halves; ++u) {
+            if (!ring_wait(b.ring_full, u, C::kSlots, wc, 0x51)) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+                const uint64_t sl = (u % C::kSlots) * kSlotDesc;
+                const uint32_t t_st = tmem + u * 2 * 64;
+                issue_st_half<D>(t_st, d_k, d_ring_k + sl);
+                issue_st_half<D>(t_st + 64, d_v, d_ring_k + sl + kHalfDesc);
+                mma_commit(b.s_full + 8 * u);
+            }
+            __syncwarp();
+        }
+        for (int u = 0; ok && u < halves; ++u) {
+            const int x = u & 1;
+            const uint32_t t_st = tmem + x * 2 * 64, t_dpt = t_st + 64;
+            if (!warp_wait(b.p_full + 8 * x, (u >> 1) & 1, wc, 0x52)) break;
+            const bool next = u + 2 < halves;
+            if (next && !ring_wait(b.ring_full, u + 2, C::kSlots, wc, 0x53)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint64_t sl = (u % C::kSlots) * kSlotDesc;
+                const uint32_t acc = u > 0 ? 1u : 0u;
+                issue_acc_half<D>(t_dv, t_st, d_ring_mn + sl + kHalfDesc, acc);   // dV += P^T dO_x
+                issue_acc_half<D>(t_dk, t_dpt, d_ring_mn + sl, acc);              // dK += dS^T Q_x
+                mma_commit(b.ring_empty + 8 * (u % C::kSlots));
+                if (next) {
+                    const uint64_t sn = ((u + 2) % C::kSlots) * kSlotDesc;
+                    issue_st_half<D>(t_st, d_k, d_ring_k + sn);
+                    issue_st_half<D>(t_dpt, d_v, d_ring_k + sn + kHalfDesc);
+                    mma_commit(b.s_full + 8 * x);
+                }
+            }
+            __syncwarp();
+        }
+        if (elect_one()) {
+            mma_commit(b.o_final);
+            mma_commit(b.drain);
+        }
+        __syncwarp();
+        mbar_drain(b.drain, 0, p.wait_limit_ns);
     } else {
         // ---------------------------------------------- P^T and dS^T
         const int r = warp * 32 + lane;           // key within the block (TMEM lane)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_off, t_dp = t_s + kT;
+        const uint32_t t_s = tmem + lane_off;
         const uint32_t t_dv = t_s + 2 * kT, t_dk = t_dv + D;
         const float c = p.scale_log2;
-        // this thread stages the row statistics of query r of each tile,
-        // loaded one tile ahead
+        const float *L = p.lse + (int64_t)unit * p.n;
+        const float *Dl = p.delta + (int64_t)unit * p.n;
+        // threads 0..63 stage the row statistics of query r of each half,
+        // loaded one half ahead
         int iq = i_first + r;
-        float nl = iq < p.n ? L[iq] * kLog2e : INFINITY, nd = iq < p.n ? Dl[iq] : 0.f;
+        float nl = 0.f, nd = 0.f;
+        if (r < 64) {
+            nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
+            nd = iq < p.n ? Dl[iq] : 0.f;
+        }
         bool ok = true;
-        for (int t = 0; t < tiles; ++t) {
-            float *sl = stat + (t % kStages) * 2 * kT, *sd = sl + kT;
-            sl[r] = nl;
-            sd[r] = nd;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            iq += kT;
-            if (t + 1 < tiles) {
-                nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
-                nd = iq < p.n ? Dl[iq] : 0.f;
+        for (int u = 0; u < halves; ++u) {
+            const int x = u & 1;
+            float *sl = stat + x * 2 * 64, *sd = sl + 64;
+            if (r < 64) {
+                sl[r] = nl;
+                sd[r] = nd;
+                iq += 64;
+                if (u + 1 < halves) {
+                    nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
+                    nd = iq < p.n ? Dl[iq] : 0.f;
+                }
             }
-            if (!warp_wait(b.s_full, t & 1, wc, 0x60)) { ok = false; break; }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const uint32_t t_st = t_s + x * 2 * 64, t_dpt = t_st + 64;
+            if (!warp_wait(b.s_full + 8 * x, (u >> 1) & 1, wc, 0x60)) { ok = false; break; }
             tc_fence_after();
-            const bool diag = p.causal && t == 0;  // query q sees key r iff q >= r
+            // causal: query q sees key r iff q >= r; only the first tile holds
+            // queries below some key of the block
+            const bool diag = p.causal && u < 2;
 #pragma unroll
-            for (int cc = 0; cc < kT / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 float sv[32], dpv[32];
-                tmem_ld32(t_s + cc * 32, sv);
-                tmem_ld32(t_dp + cc * 32, dpv);
+                tmem_ld32(t_st + cc * 32, sv);
+                tmem_ld32(t_dpt + cc * 32, dpv);
                 tmem_wait_ld();
                 uint32_t pk[16], dk[16];
+                const float2 c2 = make_float2(c, c);
 #pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    const int qi = cc * 32 + x;
-                    float p0 = ex2_approx(fmaf(sv[x], c, -sl[qi]));
-                    float p1 = ex2_approx(fmaf(sv[x + 1], c, -sl[qi + 1]));
+                for (int e = 0; e < 32; e += 4) {
+                    const int qi = cc * 32 + e;              // query within the half
+                    // the statistics of four queries: one 16-byte broadcast load each
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + qi);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + qi);
+                    const float2 a0 = __ffma2_rn(make_float2(sv[e], sv[e + 1]), c2, make_float2(-l4.x, -l4.y));
+                    const float2 a1 = __ffma2_rn(make_float2(sv[e + 2], sv[e + 3]), c2, make_float2(-l4.z, -l4.w));
+                    float2 p0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+                    float2 p1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
                     if (diag) {
-                        if (qi < r) p0 = 0.f;
-                        if (qi + 1 < r) p1 = 0.f;
+                        const int q = x * 64 + qi;
+                        if (q < r) p0.x = 0.f;
+                        if (q + 1 < r) p0.y = 0.f;
+                        if (q + 2 < r) p1.x = 0.f;
+                        if (q + 3 < r) p1.y = 0.f;
                     }
-                    pk[x / 2] = pack_bf16x2(p0, p1);
-                    dk[x / 2] = pack_bf16x2(p0 * (dpv[x] - sd[qi]), p1 * (dpv[x + 1] - sd[qi + 1]));
+                    const float2 g0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dpv[e], dpv[e + 1]), make_float2(-d4.x, -d4.y)));
+                    const float2 g1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dpv[e + 2], dpv[e + 3]), make_float2(-d4.z, -d4.w)));
+                    pk[e / 2] = pack_bf16x2(p0.x, p0.y);
+                    pk[e / 2 + 1] = pack_bf16x2(p1.x, p1.y);
+                    dk[e / 2] = pack_bf16x2(g0.x, g0.y);
+                    dk[e / 2 + 1] = pack_bf16x2(g1.x, g1.y);
                 }
-                tmem_st16(t_s + cc * 16, pk);    // P^T over S^T columns already read
-                tmem_st16(t_dp + cc * 16, dk);   // dS^T over dP^T columns already read
+                tmem_st16(t_st + cc * 16, pk);    // P^T over S^T columns already read
+                tmem_st16(t_dpt + cc * 16, dk);   // dS^T over dP^T columns already read
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b.p_full);
+            if (lane == 0) mbar_arrive(b.p_full + 8 * x);
         }
         if (ok && warp_wait(b.o_final, 0, wc, 0x61)) {
             tc_fence_after();
@@ -298,13 +459,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             Tout *dK = static_cast<Tout *>(p.dk) + ((int64_t)unit * p.n + key) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
-                float x[32];
-                tmem_ld32(t_dv + cc * 32, x);
+                float xo[32];
+                tmem_ld32(t_dv + cc * 32, xo);
                 tmem_wait_ld();
-                if (key < p.n) store_row(dV + cc * 32, x, 1.f);
-                tmem_ld32(t_dk + cc * 32, x);
+                if (key < p.n) store_row(dV + cc * 32, xo, 1.f);
+                tmem_ld32(t_dk + cc * 32, xo);
                 tmem_wait_ld();
-                if (key < p.n) store_row(dK + cc * 32, x, p.scale);
+                if (key < p.n) store_row(dK + cc * 32, xo, p.scale);
             }
         }
     }
@@ -388,16 +549,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld32(t_dp + cc * 32, dpv);
                 tmem_wait_ld();
                 uint32_t dk[16];
+                const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
+                const float2 nd2 = make_float2(-drow, -drow);
 #pragma unroll
                 for (int x = 0; x < 32; x += 2) {
-                    float p0 = ex2_approx(fmaf(sv[x], c, -lrow));
-                    float p1 = ex2_approx(fmaf(sv[x + 1], c, -lrow));
+                    const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), c2, nl2);
+                    float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                     if (need_mask) {
                         const int key = key0 + cc * 32 + x;
-                        if (key >= lim) p0 = 0.f;
-                        if (key + 1 >= lim) p1 = 0.f;
+                        if (key >= lim) pp.x = 0.f;
+                        if (key + 1 >= lim) pp.y = 0.f;
                     }
-                    dk[x / 2] = pack_bf16x2(p0 * (dpv[x] - drow), p1 * (dpv[x + 1] - drow));
+                    const float2 g = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
+                    dk[x / 2] = pack_bf16x2(g.x, g.y);
                 }
                 tmem_st16(t_s + cc * 16, dk);    // dS over S columns already read
             }
@@ -439,11 +603,12 @@ fa_status prepare(K kernel, int smem) {
 template <int D, typename Tout>
 fa_status launch(const FaBwdProblem &p) {
     using C = BCfg<D>;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tq64, tdo64;
     const uint64_t n = (uint64_t)p.n, units = (uint64_t)p.units_bh;
     const uint64_t rs = (uint64_t)D * 2, hs = n * D * 2;
     if (!make_map(&tq, p.q, D, n, units, rs, hs, kT, 1) || !make_map(&tk, p.k, D, n, units, rs, hs, kT, 1) ||
-        !make_map(&tv, p.v, D, n, units, rs, hs, kT, 1) || !make_map(&tdo, p.dout, D, n, units, rs, hs, kT, 1))
+        !make_map(&tv, p.v, D, n, units, rs, hs, kT, 1) || !make_map(&tdo, p.dout, D, n, units, rs, hs, kT, 1) ||
+        !make_map(&tq64, p.q, D, n, units, rs, hs, 64, 1) || !make_map(&tdo64, p.dout, D, n, units, rs, hs, 64, 1))
         return FA_ERR_CUDA;
     BwdTcParams k;
     k.lse = p.lse;
@@ -462,12 +627,13 @@ fa_status launch(const FaBwdProblem &p) {
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
     static bool ready = false;  // per instantiation
     if (!ready) {
-        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout>, C::kSmemBytes);
+        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout>, DkCfg<D>::kSmemBytes);
         if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout>, C::kSmemBytes);
         if (st != FA_OK) return st;
         ready = true;
     }
-    bwd_dkdv_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, C::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    bwd_dkdv_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv,
+                                                                                           tdo64, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
     bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, C::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
