@@ -17,8 +17,8 @@
 //
 // Both are made of the forward pass's two MMA shapes (A B^T with both
 // operands K-major in shared memory; A from TMEM times an MN-major shared
-// operand).  The streamed operand pair (Q_i and dO_i, or K_j and V_j) flows
-// through a two-stage TMA ring.  Warps 0-3 turn S, dP into P, dS (one TMEM
+// operand).  The streamed operands (Q_i and dO_i, or K_j and V_j) flow
+// through a TMA ring.  Warps 0-3 turn S, dP into P, dS (one TMEM
 // lane, i.e. one key or one query row, per thread), warp 4 is the TMA
 // producer, warp 5 allocates TMEM and issues the MMAs.  Every wait is
 // bounded (the device watchdog of the forward kernel).
@@ -36,22 +36,7 @@ constexpr int kT = kTcRows;          // 128 rows / keys per tile
 constexpr int kBwdThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kStages = 2;           // streamed operand pairs in flight
 constexpr uint32_t kTmemCols = 512;
-
-template <int D>
-struct BCfg {
-    static constexpr int kHalves = D / 64;
-    static constexpr int kTileBytes = kT * D * 2;
-    static constexpr int kRingOff = 2 * kTileBytes;                  // after the resident pair
-    static constexpr int kStatOff = kRingOff + 2 * kStages * kTileBytes;
-    static constexpr int kStatBytes = kStages * 2 * kT * 4;          // [stage][L, delta][128]
-    static constexpr int kBarOff = kStatOff + kStatBytes;
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;    // + alignment slack
-    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(2 * kT + 2 * D <= (int)kTmemCols, "TMEM columns");
-};
 
 struct BwdTcParams {
     const float *lse, *delta;
@@ -86,107 +71,8 @@ template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int row,
                                           int unit) {
 #pragma unroll
-    for (int hf = 0; hf < BCfg<D>::kHalves; ++hf)
+    for (int hf = 0; hf < D / 64; ++hf)
         tma_load_3d(dst + hf * kTcAtomBytes, tm, bar, hf * 64, row, unit);
-}
-
-// Barriers of the dQ kernel: fixed-pair full, ring full/empty per stage,
-// S-and-dP ready, dS ready, accumulator final, drain.
-struct Bars {
-    uint32_t fix_full, ring_full, ring_empty, s_full, p_full, o_final, drain;
-    __device__ explicit Bars(uint32_t b)
-        : fix_full(b), ring_full(b + 8), ring_empty(b + 8 + 8 * kStages), s_full(b + 8 + 16 * kStages),
-          p_full(b + 16 + 16 * kStages), o_final(b + 24 + 16 * kStages), drain(b + 32 + 16 * kStages) {}
-};
-static_assert(40 + 16 * kStages + 16 <= 256, "barrier area");
-
-__device__ __forceinline__ void init_bars(const Bars &b) {
-    mbar_init(b.fix_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-        mbar_init(b.ring_full + 8 * s, 1);
-        mbar_init(b.ring_empty + 8 * s, 1);
-    }
-    mbar_init(b.s_full, 1);
-    mbar_init(b.p_full, 4);
-    mbar_init(b.o_final, 1);
-    mbar_init(b.drain, 1);
-    fence_barrier_init();
-}
-
-// Producer: the resident pair (fixed rows), then `tiles` streamed pairs.
-template <int D>
-__device__ void produce(const Bars &b, uint32_t base, const CUtensorMap *tm_f0, const CUtensorMap *tm_f1,
-                        const CUtensorMap *tm_r0, const CUtensorMap *tm_r1, int fixed_row, int first_row,
-                        int tiles, int unit, const WaitCtx &wc, uint64_t lim) {
-    using C = BCfg<D>;
-    mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
-    load_tile<D>(base, tm_f0, b.fix_full, fixed_row, unit);
-    load_tile<D>(base + C::kTileBytes, tm_f1, b.fix_full, fixed_row, unit);
-    int t = 0;
-    for (; t < tiles; ++t) {
-        const int s = t % kStages, round = t / kStages;
-        if (round > 0 && !mbar_wait(b.ring_empty + 8 * s, (round - 1) & 1, wc, 0x41)) break;
-        const uint32_t dst = base + C::kRingOff + s * 2 * C::kTileBytes;
-        mbar_arrive_expect_tx(b.ring_full + 8 * s, 2 * C::kTileBytes);
-        load_tile<D>(dst, tm_r0, b.ring_full + 8 * s, first_row + t * kT, unit);
-        load_tile<D>(dst + C::kTileBytes, tm_r1, b.ring_full + 8 * s, first_row + t * kT, unit);
-    }
-    // Teardown: every copy issued lands before the CTA exits.
-    mbar_drain(b.fix_full, 0, lim);
-    for (int u = t > kStages ? t - kStages : 0; u < t; ++u)
-        mbar_drain(b.ring_full + 8 * (u % kStages), (u / kStages) & 1, lim);
-}
-
-// MMA warp: per streamed tile, S = F0 R0^T and dP = F1 R1^T (or the
-// transposed forms), then once P / dS are in TMEM, acc0 (+)= P R1 and
-// acc1 (+)= dS R_x with R_x the MN-major view of the streamed tile `acc1_src`
-// (0: R0, 1: R1) ... see the two callers.
-struct MmaPlan {
-    uint32_t t_s, t_dp, t_acc0, t_acc1;  // TMEM addresses
-    int acc0_b, acc1_b;                  // streamed tile feeding acc0 / acc1 (0 or 1)
-    bool two_acc;                        // dK/dV kernel: two accumulators
-};
-
-template <int D>
-__device__ void mma_role(const Bars &b, uint32_t base, const MmaPlan &m, int tiles, const WaitCtx &wc,
-                         uint64_t lim) {
-    using C = BCfg<D>;
-    constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
-    const uint64_t d_f0 = smem_desc(base, 16, 1024), d_f1 = d_f0 + kTileDesc;
-    const uint64_t d_ring_k = smem_desc(base + C::kRingOff, 16, 1024);          // K-major view
-    const uint64_t d_ring_mn = smem_desc(base + C::kRingOff, kTcAtomBytes, 1024);  // MN-major view
-    bool ok = warp_wait(b.fix_full, 0, wc, 0x50);
-    for (int t = 0; ok && t < tiles; ++t) {
-        const int s = t % kStages;
-        if (!warp_wait(b.ring_full + 8 * s, (t / kStages) & 1, wc, 0x51)) break;
-        tc_fence_after();
-        const uint64_t r0 = s * 2 * kTileDesc, r1 = r0 + kTileDesc;
-        if (elect_one()) {
-            issue_qk<D>(m.t_s, d_f0, d_ring_k + r0);
-            issue_qk<D>(m.t_dp, d_f1, d_ring_k + r1);
-            mma_commit(b.s_full);
-        }
-        __syncwarp();
-        if (!warp_wait(b.p_full, t & 1, wc, 0x52)) break;
-        tc_fence_after();
-        if (elect_one()) {
-            const uint32_t acc = t > 0 ? 1u : 0u;
-            if (m.two_acc) {
-                issue_pv<D>(m.t_acc0, m.t_s, d_ring_mn + (m.acc0_b ? r1 : r0), acc);    // dV += P^T dO
-                issue_pv<D>(m.t_acc1, m.t_dp, d_ring_mn + (m.acc1_b ? r1 : r0), acc);   // dK += dS^T Q
-            } else {
-                issue_pv<D>(m.t_acc0, m.t_s, d_ring_mn + (m.acc0_b ? r1 : r0), acc);    // dQ += dS K
-            }
-            mma_commit(b.ring_empty + 8 * s);
-        }
-        __syncwarp();
-    }
-    if (elect_one()) {
-        mma_commit(b.o_final);
-        mma_commit(b.drain);
-    }
-    __syncwarp();
-    mbar_drain(b.drain, 0, lim);
 }
 
 // ------------------------------------------------------------ dK, dV --
@@ -478,17 +364,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ --
+// Q and dO stay in shared memory; K_j and V_j stream through a ring of
+// kSlots single-tile slots (loads K_0, V_0, K_1, V_1, ...), V_j released
+// after dP_j, K_j after dQ's use of it.  Two TMEM buffers hold S (the
+// softmax warps write dS over it), one holds dP.  Per tile t the MMA warp
+// issues, once dS_t is ready:
+//   dP_{t+1} = dO V_{t+1}^T   (the dP buffer has been read)
+//   dQ += dS_t K_t
+//   S_{t+2} = Q K_{t+2}^T     (into dS_t's buffer, after dQ read it)
+// so the softmax warps' next input (S_{t+1}, computed a tile earlier, and
+// dP_{t+1}) waits for one MMA only.
+template <int D>
+struct DqCfg {
+    static constexpr int kTileBytes = kT * D * 2;
+    static constexpr int kSlots = D == 128 ? 5 : 10;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(8 * (1 + 2 * kSlots + 4) + 16 <= kBarBytes, "barrier area");
+    static_assert(3 * kT + D <= (int)kTmemCols, "TMEM columns");
+};
+
 template <int D, typename Tout>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdTcParams p) {
-    using C = BCfg<D>;
+    using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const Bars b(base + C::kBarOff);
+    const uint32_t bars = base + C::kBarOff;
+    const uint32_t fix_full = bars, kv_full = bars + 8, kv_empty = kv_full + 8 * C::kSlots;
+    const uint32_t s_full = kv_empty + 8 * C::kSlots, ds_full = s_full + 8, o_final = ds_full + 8;
+    const uint32_t drain = o_final + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -500,7 +412,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int tiles = p.causal ? min(ib + 1, key_tiles) : key_tiles;
 
     if (warp == kProdWarp && lane == 0) {
-        init_bars(b);
+        mbar_init(fix_full, 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(kv_full + 8 * i, 1);
+            mbar_init(kv_empty + 8 * i, 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(ds_full, 4);
+        mbar_init(o_final, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
         *abort_flag = 0;
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -516,27 +437,103 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
+    const uint32_t ring = base + C::kRingOff;
 
     if (warp == kProdWarp) {
-        if (lane == 0)
-            produce<D>(b, base, &tm_q, &tm_do, &tm_k, &tm_v, i0, 0, tiles, unit, wc, p.wait_limit_ns);
+        // ---------------------------------------------------- producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
+            load_tile<D>(base, &tm_q, fix_full, i0, unit);
+            load_tile<D>(base + C::kTileBytes, &tm_do, fix_full, i0, unit);
+            uint32_t li = 0;
+            bool ok = true;
+            for (int j = 0; ok && j < tiles; ++j) {
+                for (int kv = 0; kv < 2; ++kv, ++li) {
+                    const uint32_t slot = li % C::kSlots, round = li / C::kSlots;
+                    if (round > 0 && !mbar_wait(kv_empty + 8 * slot, (round - 1) & 1, wc, 0x42)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
+                    load_tile<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
+                                 j * kT, unit);
+                }
+            }
+            const uint64_t lim = p.wait_limit_ns;
+            mbar_drain(fix_full, 0, lim);
+            for (uint32_t u = li > (uint32_t)C::kSlots ? li - C::kSlots : 0; u < li; ++u)
+                mbar_drain(kv_full + 8 * (u % C::kSlots), (u / C::kSlots) & 1, lim);
+        }
     } else if (warp == kMmaWarp) {
-        // S = Q K^T, dP = dO V^T; dQ += dS K (K: streamed tile 0).  dS is
-        // written over S's columns, so the plan's "P" operand is dS here.
-        const MmaPlan m{tmem, tmem + kT, tmem + 2 * kT, 0, 0, 0, false};
-        mma_role<D>(b, base, m, tiles, wc, p.wait_limit_ns);
+        // --------------------------------------------------------- MMA
+        constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
+        const uint64_t d_q = smem_desc(base, 16, 1024), d_do = d_q + kTileDesc;
+        const uint64_t d_ring_k = smem_desc(ring, 16, 1024);
+        const uint64_t d_ring_mn = smem_desc(ring, kTcAtomBytes, 1024);
+        const uint32_t t_dp = tmem + 2 * kT, t_dq = tmem + 3 * kT;
+        // K_j is ring load 2j, V_j load 2j + 1
+        bool ok = warp_wait(fix_full, 0, wc, 0x54) && ring_wait(kv_full, 0, C::kSlots, wc, 0x55) &&
+                  ring_wait(kv_full, 1, C::kSlots, wc, 0x55);
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                issue_qk<D>(tmem, d_q, d_ring_k);                                  // S_0
+                issue_qk<D>(t_dp, d_do, d_ring_k + 1 * kTileDesc);                 // dP_0
+                mma_commit(s_full);
+                mma_commit(kv_empty + 8 * 1);                                      // V_0 read
+            }
+            __syncwarp();
+        }
+        if (ok && tiles > 1) {
+            ok = ring_wait(kv_full, 2, C::kSlots, wc, 0x55);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) issue_qk<D>(tmem + kT, d_q, d_ring_k + (2 % C::kSlots) * kTileDesc);  // S_1
+                __syncwarp();
+            }
+        }
+        for (int t = 0; ok && t < tiles; ++t) {
+            const uint32_t t_buf = tmem + (t & 1) * kT;
+            if (!warp_wait(ds_full, t & 1, wc, 0x56)) break;
+            const uint32_t lk = 2 * t, lvn = 2 * t + 3, lk2 = 2 * t + 4;
+            if (t + 1 < tiles && !ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                if (t + 1 < tiles) {
+                    issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
+                    mma_commit(s_full);
+                    mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+                }
+                issue_pv<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
+                mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
+            }
+            __syncwarp();
+            if (t + 2 < tiles) {
+                if (!ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) break;
+                tc_fence_after();
+                if (elect_one()) issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
+                __syncwarp();
+            }
+        }
+        if (elect_one()) {
+            mma_commit(o_final);
+            mma_commit(drain);
+        }
+        __syncwarp();
+        mbar_drain(drain, 0, p.wait_limit_ns);
     } else {
         // ------------------------------------------------------- dS
         const int r = warp * 32 + lane;           // query row within the block (TMEM lane)
         const int row = i0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_off, t_dp = t_s + kT, t_dq = t_s + 2 * kT;
+        const uint32_t t_s0 = tmem + lane_off, t_dp = t_s0 + 2 * kT, t_dq = t_s0 + 3 * kT;
         const float c = p.scale_log2;
         const float lrow = row < p.n ? p.lse[(int64_t)unit * p.n + row] * kLog2e : INFINITY;
         const float drow = row < p.n ? p.delta[(int64_t)unit * p.n + row] : 0.f;
         bool ok = true;
         for (int t = 0; t < tiles; ++t) {
-            if (!warp_wait(b.s_full, t & 1, wc, 0x70)) { ok = false; break; }
+            const uint32_t t_s = t_s0 + (t & 1) * kT;
+            if (!warp_wait(s_full, t & 1, wc, 0x70)) { ok = false; break; }
             tc_fence_after();
             const int key0 = t * kT;
             // keys past the causal diagonal or past the end are masked
@@ -568,9 +565,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b.p_full);
+            if (lane == 0) mbar_arrive(ds_full);
         }
-        if (ok && warp_wait(b.o_final, 0, wc, 0x71)) {
+        if (ok && warp_wait(o_final, 0, wc, 0x71)) {
             tc_fence_after();
             Tout *dQ = static_cast<Tout *>(p.dq) + ((int64_t)unit * p.n + row) * D;
 #pragma unroll
@@ -602,7 +599,6 @@ fa_status prepare(K kernel, int smem) {
 
 template <int D, typename Tout>
 fa_status launch(const FaBwdProblem &p) {
-    using C = BCfg<D>;
     CUtensorMap tq, tk, tv, tdo, tq64, tdo64;
     const uint64_t n = (uint64_t)p.n, units = (uint64_t)p.units_bh;
     const uint64_t rs = (uint64_t)D * 2, hs = n * D * 2;
@@ -628,7 +624,7 @@ fa_status launch(const FaBwdProblem &p) {
     static bool ready = false;  // per instantiation
     if (!ready) {
         fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout>, DkCfg<D>::kSmemBytes);
-        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout>, C::kSmemBytes);
+        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout>, DqCfg<D>::kSmemBytes);
         if (st != FA_OK) return st;
         ready = true;
     }
@@ -636,7 +632,7 @@ fa_status launch(const FaBwdProblem &p) {
                                                                                            tdo64, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, C::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
     e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
