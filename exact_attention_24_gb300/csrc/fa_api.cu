@@ -278,19 +278,16 @@ size_t fa_bwd_workspace_size(int B, int H, int N) {
     return (rows * sizeof(float) + 255) / 256 * 256;
 }
 
-fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
-                 const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
-                 float scale, int causal, fa_dtype dtype, void *workspace,
-                 size_t workspace_bytes, fa_stream_t stream) {
-    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+// Checks shared by the backward entry points; `rows` = heads * tokens.
+static fa_status check_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                           const float *L, void *dQ, void *dK, void *dV, int64_t rows, int D,
+                           float scale, int causal, fa_dtype dtype, void *workspace,
+                           size_t workspace_bytes) {
     if (D <= 0) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_BF16_OUT_F32) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-    const int64_t units = (int64_t)B * H;
-    if (units > INT32_MAX || (int64_t)N > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
-    const int64_t rows = units * N;
     if (rows == 0) return FA_OK;
     const void *ins[6] = {Q, K, V, O, dO, L};
     void *outs[3] = {dQ, dK, dV};
@@ -298,11 +295,10 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARG;
     for (const void *x : outs)
         if (!x || !aligned16(x)) return FA_ERR_INVALID_ARG;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fa_bwd_workspace_size(B, H, N))
-        return FA_ERR_INVALID_ARG;
+    const size_t nw = (size_t)rows * sizeof(float);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < nw) return FA_ERR_INVALID_ARG;
     const size_t ni = (size_t)rows * D * in_bytes(dtype), no = (size_t)rows * D * out_bytes(dtype);
-    const size_t nl = (size_t)rows * sizeof(float), nw = (size_t)rows * sizeof(float);
-    const size_t in_sizes[6] = {ni, ni, ni, ni, ni, nl};
+    const size_t in_sizes[6] = {ni, ni, ni, ni, ni, nw};
     for (int a = 0; a < 3; ++a) {
         for (int b = 0; b < 6; ++b)
             if (overlaps(outs[a], no, ins[b], in_sizes[b])) return FA_ERR_INVALID_ARG;
@@ -312,7 +308,39 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     }
     for (int b = 0; b < 6; ++b)
         if (overlaps(workspace, nw, ins[b], in_sizes[b])) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
 
+static fa_status run_bwd(FaBwdProblem &p) {
+    p.err = err_word();
+    if (!p.err) return FA_ERR_CUDA;
+    p.grid_ctas = g_opts.grid_ctas;
+    p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
+    fa_status st = fa_launch_bwd_delta(p);
+    if (st != FA_OK) return st;
+    const bool bf16 = p.dtype != FA_F32;
+    switch (g_opts.kernel) {
+        case FA_KERNEL_SIMT: return fa_launch_bwd_simt(p);
+        case FA_KERNEL_TC: return bf16 ? fa_launch_bwd_tc(p) : FA_ERR_UNSUPPORTED;
+        default:
+            if (!bf16) return fa_launch_bwd_simt(p);
+            st = fa_launch_bwd_tc(p);
+            return st == FA_ERR_UNSUPPORTED ? fa_launch_bwd_simt(p) : st;
+    }
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                 float scale, int causal, fa_dtype dtype, void *workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    const int64_t units = (int64_t)B * H;
+    if (units > INT32_MAX || (int64_t)N > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    const int64_t rows = units * N;
+    fa_status st = check_bwd(Q, K, V, O, dO, L, dQ, dK, dV, rows, D, scale, causal, dtype,
+                             workspace, workspace_bytes);
+    if (st != FA_OK || rows == 0) return st;
+    if (workspace_bytes < fa_bwd_workspace_size(B, H, N)) return FA_ERR_INVALID_ARG;
     FaBwdProblem p{};
     p.q = Q;
     p.k = K;
@@ -324,8 +352,10 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     p.dk = dK;
     p.dv = dV;
     p.delta = static_cast<float *>(workspace);
+    p.heads = H;
     p.units_bh = (int)units;
     p.n = N;
+    p.total = N;
     p.D = D;
     p.scale = scale;
     p.causal = causal;
@@ -333,21 +363,53 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     p.wr = causal ? 0 : -1;
     p.dtype = dtype;
     p.stream = static_cast<cudaStream_t>(stream);
-    p.err = err_word();
-    if (!p.err) return FA_ERR_CUDA;
-    p.grid_ctas = g_opts.grid_ctas;
-    p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
-    fa_status st = fa_launch_bwd_delta(p);
+    return run_bwd(p);
+}
+
+size_t fa_bwd_varlen_workspace_size(int total_tokens, int H) {
+    if (total_tokens <= 0 || H <= 0) return 0;
+    return ((size_t)total_tokens * (size_t)H * sizeof(float) + 255) / 256 * 256;
+}
+
+fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        const float *L, void *dQ, void *dK, void *dV, const int32_t *cu_seqlens,
+                        int num_seqs, int total_tokens, int max_seqlen, int H, int D, float scale,
+                        int causal, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                        fa_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H < 0) return FA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)total_tokens * H;
+    fa_status st = check_bwd(Q, K, V, O, dO, L, dQ, dK, dV, rows, D, scale, causal, dtype,
+                             workspace, workspace_bytes);
     if (st != FA_OK) return st;
-    const bool bf16 = dtype != FA_F32;
-    switch (g_opts.kernel) {
-        case FA_KERNEL_SIMT: return fa_launch_bwd_simt(p);
-        case FA_KERNEL_TC: return bf16 ? fa_launch_bwd_tc(p) : FA_ERR_UNSUPPORTED;
-        default:
-            if (!bf16) return fa_launch_bwd_simt(p);
-            st = fa_launch_bwd_tc(p);
-            return st == FA_ERR_UNSUPPORTED ? fa_launch_bwd_simt(p) : st;
-    }
+    if (num_seqs == 0 || rows == 0 || max_seqlen == 0) return FA_OK;
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * H > INT32_MAX || max_seqlen > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    FaBwdProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.dout = dO;
+    p.lse = L;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.delta = static_cast<float *>(workspace);
+    p.cu_seqlens = cu_seqlens;
+    p.varlen = 1;
+    p.heads = H;
+    p.num_seqs = num_seqs;
+    p.units_bh = num_seqs * H;
+    p.n = max_seqlen;
+    p.total = total_tokens;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.wl = -1;
+    p.wr = causal ? 0 : -1;
+    p.dtype = dtype;
+    p.stream = static_cast<cudaStream_t>(stream);
+    return run_bwd(p);
 }
 
 fa_status fa_check_device_error(fa_stream_t stream) {

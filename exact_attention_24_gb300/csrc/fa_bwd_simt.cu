@@ -36,10 +36,42 @@ struct BwdParams {
     const void *q, *k, *v, *o, *dout;
     const float *lse, *delta;
     void *dq, *dk, *dv;
+    const int32_t *cu;
+    int varlen, heads, num_seqs;
+    int64_t total;
     int n, D;
     float scale;
     int causal, wl, wr;
+    uint32_t *err;
 };
+
+// One attention problem of the batch: (batch, head) of a dense batch or
+// (sequence, head) of a packed one.  Row i of its Q (K, V, ...) starts at
+// element elem0 + i * rstride; its L and delta at stat0 + i.
+struct Head {
+    int64_t elem0, rstride, stat0;
+    int len;
+};
+
+__device__ __forceinline__ Head head_of(const BwdParams &p, int unit, int D) {
+    Head h;
+    if (!p.varlen) {
+        h.elem0 = (int64_t)unit * p.n * D;
+        h.rstride = D;
+        h.stat0 = (int64_t)unit * p.n;
+        h.len = p.n;
+    } else {
+        const int s = unit / p.heads, hh = unit % p.heads;
+        int64_t start;
+        int len;
+        seq_bounds(p.cu, s, p.total, p.n, p.err, start, len);  // invalid: len = 0
+        h.elem0 = (start * p.heads + hh) * D;
+        h.rstride = (int64_t)p.heads * D;
+        h.stat0 = (int64_t)hh * p.total + start;
+        h.len = len;
+    }
+    return h;
+}
 
 __device__ __forceinline__ float ldf(const float *p) { return *p; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
@@ -59,10 +91,12 @@ __device__ __forceinline__ bool visible(int i, int j, const BwdParams &p) {
     return true;
 }
 
-// delta[row] = sum_c dO[row, c] * O[row, c]; one warp per row.
+// delta = sum_c dO[row, c] * O[row, c]; one warp per row.  Rows are taken
+// in memory order; a packed batch ([total, H, D]) stores row t*H + h's
+// statistic at h*total + t, like L.
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const T *o, const T *dout, float *delta,
-                                                        int64_t rows, int D) {
+                                                        int64_t rows, int D, int heads, int64_t total) {
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -70,15 +104,16 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const T *o, const T *dou
     float s = 0.f;
     for (int c = lane; c < D; c += 32) s = fmaf(ldf(a + c), ldf(b + c), s);
     s = wsum(s);
-    if (lane == 0) delta[row] = s;
+    if (lane == 0) delta[heads > 0 ? (row % heads) * total + row / heads : row] = s;
 }
 
-// Rows [r0, r0 + kTile) of a head into shared memory as float32 (zero past n).
+// Rows [r0, r0 + kTile) of a head (row stride rs elements) into shared
+// memory as float32 (zero past n).
 template <int D, typename T>
-__device__ __forceinline__ void stage(float *dst, const T *src, int r0, int n) {
+__device__ __forceinline__ void stage(float *dst, const T *src, int64_t rs, int r0, int n) {
     for (int x = threadIdx.x; x < kTile * D; x += blockDim.x) {
         const int r = x / D, c = x % D;
-        dst[x] = r0 + r < n ? ldf(src + (int64_t)(r0 + r) * D + c) : 0.f;
+        dst[x] = r0 + r < n ? ldf(src + (int64_t)(r0 + r) * rs + c) : 0.f;
     }
 }
 
@@ -91,12 +126,15 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(BwdParams p,
     __shared__ float sl[kTile], sd[kTile];
     const int bh = blockIdx.x / nblk, j0 = (blockIdx.x % nblk) * kBlock;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t base = (int64_t)bh * p.n;
-    const Tin *Q = static_cast<const Tin *>(p.q) + base * D;
-    const Tin *K = static_cast<const Tin *>(p.k) + base * D;
-    const Tin *V = static_cast<const Tin *>(p.v) + base * D;
-    const Tin *dO = static_cast<const Tin *>(p.dout) + base * D;
-    const float *L = p.lse + base, *Dl = p.delta + base;
+    const Head hd = head_of(p, bh, D);
+    if (j0 >= hd.len) return;
+    const int n = hd.len;
+    const int64_t rs = hd.rstride;
+    const Tin *Q = static_cast<const Tin *>(p.q) + hd.elem0;
+    const Tin *K = static_cast<const Tin *>(p.k) + hd.elem0;
+    const Tin *V = static_cast<const Tin *>(p.v) + hd.elem0;
+    const Tin *dO = static_cast<const Tin *>(p.dout) + hd.elem0;
+    const float *L = p.lse + hd.stat0, *Dl = p.delta + hd.stat0;
 
     float kr[kPerWarp][C], vr[kPerWarp][C], dk[kPerWarp][C], dv[kPerWarp][C];
     int jk[kPerWarp];
@@ -107,25 +145,25 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(BwdParams p,
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             const int col = lane + 32 * c;
-            kr[t][c] = j < p.n ? ldf(K + (int64_t)j * D + col) : 0.f;
-            vr[t][c] = j < p.n ? ldf(V + (int64_t)j * D + col) : 0.f;
+            kr[t][c] = j < n ? ldf(K + (int64_t)j * rs + col) : 0.f;
+            vr[t][c] = j < n ? ldf(V + (int64_t)j * rs + col) : 0.f;
             dk[t][c] = dv[t][c] = 0.f;
         }
     }
     // rows that can see some key of this block
     const int jl = j0 + kBlock - 1;
-    int i_lo = 0, i_hi = p.n;
+    int i_lo = 0, i_hi = n;
     if (p.causal) i_lo = j0;
     if (p.wr >= 0) i_lo = max(i_lo, j0 - p.wr);
     if (p.wl >= 0) i_hi = min(i_hi, jl + p.wl + 1);
     for (int i0 = i_lo; i0 < i_hi; i0 += kTile) {
         __syncthreads();
-        stage<D>(sq, Q, i0, p.n);
-        stage<D>(sdo, dO, i0, p.n);
+        stage<D>(sq, Q, rs, i0, n);
+        stage<D>(sdo, dO, rs, i0, n);
         if (threadIdx.x < kTile) {
             const int i = i0 + threadIdx.x;
-            sl[threadIdx.x] = i < p.n ? L[i] : 0.f;
-            sd[threadIdx.x] = i < p.n ? Dl[i] : 0.f;
+            sl[threadIdx.x] = i < n ? L[i] : 0.f;
+            sd[threadIdx.x] = i < n ? Dl[i] : 0.f;
         }
         __syncthreads();
         const int rows = min(kTile, i_hi - i0);
@@ -139,7 +177,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(BwdParams p,
             }
 #pragma unroll
             for (int t = 0; t < kPerWarp; ++t) {
-                if (jk[t] >= p.n || !visible(i, jk[t], p)) continue;
+                if (jk[t] >= n || !visible(i, jk[t], p)) continue;
                 float s = 0.f, dp = 0.f;
 #pragma unroll
                 for (int c = 0; c < C; ++c) {
@@ -158,16 +196,16 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(BwdParams p,
             }
         }
     }
-    Tout *dK = static_cast<Tout *>(p.dk) + base * D;
-    Tout *dV = static_cast<Tout *>(p.dv) + base * D;
+    Tout *dK = static_cast<Tout *>(p.dk) + hd.elem0;
+    Tout *dV = static_cast<Tout *>(p.dv) + hd.elem0;
 #pragma unroll
     for (int t = 0; t < kPerWarp; ++t) {
-        if (jk[t] >= p.n) continue;
+        if (jk[t] >= n) continue;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             const int col = lane + 32 * c;
-            stf(dK + (int64_t)jk[t] * D + col, p.scale * dk[t][c]);
-            stf(dV + (int64_t)jk[t] * D + col, dv[t][c]);
+            stf(dK + (int64_t)jk[t] * rs + col, p.scale * dk[t][c]);
+            stf(dV + (int64_t)jk[t] * rs + col, dv[t][c]);
         }
     }
 }
@@ -180,12 +218,15 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(BwdParams p, i
     __shared__ float sk[kTile * D], sv[kTile * D];
     const int bh = blockIdx.x / nblk, i0 = (nblk - 1 - blockIdx.x % nblk) * kBlock;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t base = (int64_t)bh * p.n;
-    const Tin *Q = static_cast<const Tin *>(p.q) + base * D;
-    const Tin *K = static_cast<const Tin *>(p.k) + base * D;
-    const Tin *V = static_cast<const Tin *>(p.v) + base * D;
-    const Tin *dO = static_cast<const Tin *>(p.dout) + base * D;
-    const float *L = p.lse + base, *Dl = p.delta + base;
+    const Head hd = head_of(p, bh, D);
+    if (i0 >= hd.len) return;
+    const int n = hd.len;
+    const int64_t rs = hd.rstride;
+    const Tin *Q = static_cast<const Tin *>(p.q) + hd.elem0;
+    const Tin *K = static_cast<const Tin *>(p.k) + hd.elem0;
+    const Tin *V = static_cast<const Tin *>(p.v) + hd.elem0;
+    const Tin *dO = static_cast<const Tin *>(p.dout) + hd.elem0;
+    const float *L = p.lse + hd.stat0, *Dl = p.delta + hd.stat0;
 
     float qr[kPerWarp][C], dor[kPerWarp][C], dq[kPerWarp][C], li[kPerWarp], di[kPerWarp];
     int ir[kPerWarp];
@@ -193,25 +234,25 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(BwdParams p, i
     for (int t = 0; t < kPerWarp; ++t) {
         const int i = i0 + warp * kPerWarp + t;
         ir[t] = i;
-        li[t] = i < p.n ? L[i] : 0.f;
-        di[t] = i < p.n ? Dl[i] : 0.f;
+        li[t] = i < n ? L[i] : 0.f;
+        di[t] = i < n ? Dl[i] : 0.f;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             const int col = lane + 32 * c;
-            qr[t][c] = i < p.n ? ldf(Q + (int64_t)i * D + col) : 0.f;
-            dor[t][c] = i < p.n ? ldf(dO + (int64_t)i * D + col) : 0.f;
+            qr[t][c] = i < n ? ldf(Q + (int64_t)i * rs + col) : 0.f;
+            dor[t][c] = i < n ? ldf(dO + (int64_t)i * rs + col) : 0.f;
             dq[t][c] = 0.f;
         }
     }
-    const int il = min(p.n, i0 + kBlock) - 1;
-    int j_lo = 0, j_hi = p.n;
+    const int il = min(n, i0 + kBlock) - 1;
+    int j_lo = 0, j_hi = n;
     if (p.causal) j_hi = il + 1;
     if (p.wr >= 0) j_hi = min(j_hi, il + p.wr + 1);
     if (p.wl >= 0) j_lo = max(0, i0 - p.wl);
     for (int j0 = j_lo; j0 < j_hi; j0 += kTile) {
         __syncthreads();
-        stage<D>(sk, K, j0, p.n);
-        stage<D>(sv, V, j0, p.n);
+        stage<D>(sk, K, rs, j0, n);
+        stage<D>(sv, V, rs, j0, n);
         __syncthreads();
         const int keys = min(kTile, j_hi - j0);
         for (int x = 0; x < keys; ++x) {
@@ -224,7 +265,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(BwdParams p, i
             }
 #pragma unroll
             for (int t = 0; t < kPerWarp; ++t) {
-                if (ir[t] >= p.n || !visible(ir[t], j, p)) continue;
+                if (ir[t] >= n || !visible(ir[t], j, p)) continue;
                 float s = 0.f, dp = 0.f;
 #pragma unroll
                 for (int c = 0; c < C; ++c) {
@@ -240,12 +281,12 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(BwdParams p, i
             }
         }
     }
-    Tout *dQ = static_cast<Tout *>(p.dq) + base * D;
+    Tout *dQ = static_cast<Tout *>(p.dq) + hd.elem0;
 #pragma unroll
     for (int t = 0; t < kPerWarp; ++t) {
-        if (ir[t] >= p.n) continue;
+        if (ir[t] >= n) continue;
 #pragma unroll
-        for (int c = 0; c < C; ++c) stf(dQ + (int64_t)ir[t] * D + lane + 32 * c, p.scale * dq[t][c]);
+        for (int c = 0; c < C; ++c) stf(dQ + (int64_t)ir[t] * rs + lane + 32 * c, p.scale * dq[t][c]);
     }
 }
 
@@ -261,6 +302,12 @@ BwdParams make_params(const FaBwdProblem &p) {
     k.dq = p.dq;
     k.dk = p.dk;
     k.dv = p.dv;
+    k.cu = p.cu_seqlens;
+    k.varlen = p.varlen;
+    k.heads = p.heads;
+    k.num_seqs = p.num_seqs;
+    k.total = p.total;
+    k.err = p.err;
     k.n = p.n;
     k.D = p.D;
     k.scale = p.scale;
@@ -298,17 +345,19 @@ fa_status launch_d(const FaBwdProblem &p) {
 }  // namespace fa
 
 fa_status fa_launch_bwd_delta(const FaBwdProblem &p) {
-    const int64_t rows = (int64_t)p.units_bh * p.n;
+    const int64_t rows = p.varlen ? p.total * p.heads : (int64_t)p.units_bh * p.n;
+    const int heads = p.varlen ? p.heads : 0;
     if (rows == 0) return FA_OK;
     const int64_t grid = (rows + 7) / 8;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
     if (p.dtype == FA_F32)
         fa::bwd_delta_kernel<float><<<(int)grid, 256, 0, p.stream>>>(
-            static_cast<const float *>(p.o), static_cast<const float *>(p.dout), p.delta, rows, p.D);
+            static_cast<const float *>(p.o), static_cast<const float *>(p.dout), p.delta, rows, p.D, heads,
+            p.total);
     else
         fa::bwd_delta_kernel<__nv_bfloat16><<<(int)grid, 256, 0, p.stream>>>(
             static_cast<const __nv_bfloat16 *>(p.o), static_cast<const __nv_bfloat16 *>(p.dout),
-            p.delta, rows, p.D);
+            p.delta, rows, p.D, heads, p.total);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }

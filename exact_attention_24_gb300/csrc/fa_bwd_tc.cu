@@ -41,7 +41,10 @@ constexpr uint32_t kTmemCols = 512;
 struct BwdTcParams {
     const float *lse, *delta;
     void *dq, *dk, *dv;
-    int n, nblk;
+    const int32_t *cu;    // packed batch: sequence offsets (null for dense)
+    int varlen, heads;
+    int64_t total;
+    int n, nblk;          // n: N, or the longest sequence of a packed batch
     float scale, scale_log2;
     int causal;
     uint32_t *err;
@@ -66,13 +69,48 @@ __device__ __forceinline__ void store_row(__nv_bfloat16 *dst, const float *x, fl
                           pack_bf16x2(x[8 * i + 6] * mul, x[8 * i + 7] * mul));
 }
 
-// TMA: one 128-row tile (all D columns) of a [units][n][D] bf16 tensor.
+// One attention problem of the batch -- (batch, head) of a dense [B, H, N, D]
+// batch or (sequence, head) of a packed [total, H, D] one: row i of its
+// tensors starts at element elem0 + i * rstride, its L / delta entry is at
+// stat0 + i, and TMA addresses it as (unit, row) or (head, start + row).
+struct Seq {
+    int64_t elem0, rstride, stat0, start;
+    int len, h, unit;
+};
+
+__device__ __forceinline__ Seq seq_of(const BwdTcParams &p, int unit, int D) {
+    Seq q;
+    q.unit = unit;
+    if (!p.varlen) {
+        q.start = 0;
+        q.h = 0;
+        q.len = p.n;
+        q.elem0 = (int64_t)unit * p.n * D;
+        q.rstride = D;
+        q.stat0 = (int64_t)unit * p.n;
+    } else {
+        const int s = unit / p.heads;
+        q.h = unit % p.heads;
+        seq_bounds(p.cu, s, p.total, p.n, p.err, q.start, q.len);  // invalid: len = 0
+        q.elem0 = (q.start * p.heads + q.h) * D;
+        q.rstride = (int64_t)p.heads * D;
+        q.stat0 = (int64_t)q.h * p.total + q.start;
+    }
+    return q;
+}
+
+// TMA: rows [row, row + box) (all D columns) of one problem's tensor; a box
+// is 64 columns wide, `atom` bytes per 64-column group in shared memory.
 template <int D>
-__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int row,
-                                          int unit) {
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int row,
+                                          const Seq &q, int varlen, int atom) {
 #pragma unroll
-    for (int hf = 0; hf < D / 64; ++hf)
-        tma_load_3d(dst + hf * kTcAtomBytes, tm, bar, hf * 64, row, unit);
+    for (int hf = 0; hf < D / 64; ++hf) {
+        if (varlen)
+            tma_load_3d(dst + hf * atom, tm, bar, hf * 64, q.h, (int)(q.start + row));
+        else
+            tma_load_3d(dst + hf * atom, tm, bar, hf * 64, row, q.unit);
+    }
 }
 
 // ------------------------------------------------------------ dK, dV --
@@ -155,8 +193,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const int unit = blockIdx.x / p.nblk, jb = blockIdx.x % p.nblk;  // lowest key block first
     const int j0 = jb * kT;
+    const Seq sq = seq_of(p, unit, D);
+    if (j0 >= sq.len) return;  // block past the end of this sequence (packed batch)
+    const int n = sq.len;
     const int i_first = p.causal ? j0 : 0;
-    const int halves = 2 * ((p.n - i_first + kT - 1) / kT);
+    const int halves = 2 * ((n - i_first + kT - 1) / kT);
 
     if (warp == kProdWarp && lane == 0) {
         mbar_init(b.fix_full, 1);
@@ -192,19 +233,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ---------------------------------------------------- producer
         if (lane == 0) {
             mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
-            load_tile<D>(base, &tm_k, b.fix_full, j0, unit);
-            load_tile<D>(base + C::kTileBytes, &tm_v, b.fix_full, j0, unit);
+            load_rows<D>(base, &tm_k, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
+            load_rows<D>(base + C::kTileBytes, &tm_v, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
             int u = 0;
             for (; u < halves; ++u) {
                 const int slot = u % C::kSlots, round = u / C::kSlots;
                 if (round > 0 && !mbar_wait(b.ring_empty + 8 * slot, (round - 1) & 1, wc, 0x41)) break;
                 const uint32_t dst = ring + slot * C::kSlotBytes, fb = b.ring_full + 8 * slot;
                 mbar_arrive_expect_tx(fb, C::kSlotBytes);
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    tma_load_3d(dst + hf * C::kHalfAtom, &tm_q, fb, hf * 64, i_first + 64 * u, unit);
-                    tma_load_3d(dst + C::kHalfBytes + hf * C::kHalfAtom, &tm_do, fb, hf * 64,
-                                i_first + 64 * u, unit);
-                }
+                load_rows<D>(dst, &tm_q, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
+                load_rows<D>(dst + C::kHalfBytes, &tm_do, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
             }
             const uint64_t lim = p.wait_limit_ns;
             mbar_drain(b.fix_full, 0, lim);
@@ -268,15 +306,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t t_s = tmem + lane_off;
         const uint32_t t_dv = t_s + 2 * kT, t_dk = t_dv + D;
         const float c = p.scale_log2;
-        const float *L = p.lse + (int64_t)unit * p.n;
-        const float *Dl = p.delta + (int64_t)unit * p.n;
+        const float *L = p.lse + sq.stat0;
+        const float *Dl = p.delta + sq.stat0;
         // threads 0..63 stage the row statistics of query r of each half,
         // loaded one half ahead
         int iq = i_first + r;
         float nl = 0.f, nd = 0.f;
         if (r < 64) {
-            nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
-            nd = iq < p.n ? Dl[iq] : 0.f;
+            nl = iq < n ? L[iq] * kLog2e : INFINITY;
+            nd = iq < n ? Dl[iq] : 0.f;
         }
         bool ok = true;
         for (int u = 0; u < halves; ++u) {
@@ -287,8 +325,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 sd[r] = nd;
                 iq += 64;
                 if (u + 1 < halves) {
-                    nl = iq < p.n ? L[iq] * kLog2e : INFINITY;
-                    nd = iq < p.n ? Dl[iq] : 0.f;
+                    nl = iq < n ? L[iq] * kLog2e : INFINITY;
+                    nd = iq < n ? Dl[iq] : 0.f;
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -341,17 +379,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok && warp_wait(b.o_final, 0, wc, 0x61)) {
             tc_fence_after();
             const int key = j0 + r;
-            Tout *dV = static_cast<Tout *>(p.dv) + ((int64_t)unit * p.n + key) * D;
-            Tout *dK = static_cast<Tout *>(p.dk) + ((int64_t)unit * p.n + key) * D;
+            Tout *dV = static_cast<Tout *>(p.dv) + sq.elem0 + key * sq.rstride;
+            Tout *dK = static_cast<Tout *>(p.dk) + sq.elem0 + key * sq.rstride;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float xo[32];
                 tmem_ld32(t_dv + cc * 32, xo);
                 tmem_wait_ld();
-                if (key < p.n) store_row(dV + cc * 32, xo, 1.f);
+                if (key < n) store_row(dV + cc * 32, xo, 1.f);
                 tmem_ld32(t_dk + cc * 32, xo);
                 tmem_wait_ld();
-                if (key < p.n) store_row(dK + cc * 32, xo, p.scale);
+                if (key < n) store_row(dK + cc * 32, xo, p.scale);
             }
         }
     }
@@ -408,7 +446,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int unit = blockIdx.x / p.nblk;
     const int ib = p.nblk - 1 - blockIdx.x % p.nblk;  // highest query block first
     const int i0 = ib * kT;
-    const int key_tiles = (p.n + kT - 1) / kT;
+    const Seq sq = seq_of(p, unit, D);
+    if (i0 >= sq.len) return;  // block past the end of this sequence (packed batch)
+    const int n = sq.len;
+    const int key_tiles = (n + kT - 1) / kT;
     const int tiles = p.causal ? min(ib + 1, key_tiles) : key_tiles;
 
     if (warp == kProdWarp && lane == 0) {
@@ -443,8 +484,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ---------------------------------------------------- producer
         if (lane == 0) {
             mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
-            load_tile<D>(base, &tm_q, fix_full, i0, unit);
-            load_tile<D>(base + C::kTileBytes, &tm_do, fix_full, i0, unit);
+            load_rows<D>(base, &tm_q, fix_full, i0, sq, p.varlen, kTcAtomBytes);
+            load_rows<D>(base + C::kTileBytes, &tm_do, fix_full, i0, sq, p.varlen, kTcAtomBytes);
             uint32_t li = 0;
             bool ok = true;
             for (int j = 0; ok && j < tiles; ++j) {
@@ -455,8 +496,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
-                    load_tile<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
-                                 j * kT, unit);
+                    load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
+                                 j * kT, sq, p.varlen, kTcAtomBytes);
                 }
             }
             const uint64_t lim = p.wait_limit_ns;
@@ -528,8 +569,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t t_s0 = tmem + lane_off, t_dp = t_s0 + 2 * kT, t_dq = t_s0 + 3 * kT;
         const float c = p.scale_log2;
-        const float lrow = row < p.n ? p.lse[(int64_t)unit * p.n + row] * kLog2e : INFINITY;
-        const float drow = row < p.n ? p.delta[(int64_t)unit * p.n + row] : 0.f;
+        const float lrow = row < n ? p.lse[sq.stat0 + row] * kLog2e : INFINITY;
+        const float drow = row < n ? p.delta[sq.stat0 + row] : 0.f;
         bool ok = true;
         for (int t = 0; t < tiles; ++t) {
             const uint32_t t_s = t_s0 + (t & 1) * kT;
@@ -537,7 +578,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             const int key0 = t * kT;
             // keys past the causal diagonal or past the end are masked
-            const int lim = p.causal ? min(row + 1, p.n) : p.n;
+            const int lim = p.causal ? min(row + 1, n) : n;
             const bool need_mask = key0 + kT > lim;
 #pragma unroll
             for (int cc = 0; cc < kT / 32; ++cc) {
@@ -569,13 +610,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (ok && warp_wait(o_final, 0, wc, 0x71)) {
             tc_fence_after();
-            Tout *dQ = static_cast<Tout *>(p.dq) + ((int64_t)unit * p.n + row) * D;
+            Tout *dQ = static_cast<Tout *>(p.dq) + sq.elem0 + row * sq.rstride;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float x[32];
                 tmem_ld32(t_dq + cc * 32, x);
                 tmem_wait_ld();
-                if (row < p.n) store_row(dQ + cc * 32, x, p.scale);
+                if (row < n) store_row(dQ + cc * 32, x, p.scale);
             }
         }
     }
@@ -599,12 +640,18 @@ fa_status prepare(K kernel, int smem) {
 
 template <int D, typename Tout>
 fa_status launch(const FaBwdProblem &p) {
+    // dense: dims {D, N, B*H}, a box is {64, rows, 1}; packed: dims
+    // {D, H, total}, a box is {64, 1, rows}
     CUtensorMap tq, tk, tv, tdo, tq64, tdo64;
-    const uint64_t n = (uint64_t)p.n, units = (uint64_t)p.units_bh;
-    const uint64_t rs = (uint64_t)D * 2, hs = n * D * 2;
-    if (!make_map(&tq, p.q, D, n, units, rs, hs, kT, 1) || !make_map(&tk, p.k, D, n, units, rs, hs, kT, 1) ||
-        !make_map(&tv, p.v, D, n, units, rs, hs, kT, 1) || !make_map(&tdo, p.dout, D, n, units, rs, hs, kT, 1) ||
-        !make_map(&tq64, p.q, D, n, units, rs, hs, 64, 1) || !make_map(&tdo64, p.dout, D, n, units, rs, hs, 64, 1))
+    const uint64_t rb = (uint64_t)D * 2;
+    const uint64_t d1 = p.varlen ? (uint64_t)p.heads : (uint64_t)p.n;
+    const uint64_t d2 = p.varlen ? (uint64_t)p.total : (uint64_t)p.units_bh;
+    const uint64_t s2 = d1 * rb;
+    auto map = [&](CUtensorMap *m, const void *ptr, uint32_t rows) {
+        return p.varlen ? make_map(m, ptr, D, d1, d2, rb, s2, 1, rows) : make_map(m, ptr, D, d1, d2, rb, s2, rows, 1);
+    };
+    if (!map(&tq, p.q, kT) || !map(&tk, p.k, kT) || !map(&tv, p.v, kT) || !map(&tdo, p.dout, kT) ||
+        !map(&tq64, p.q, 64) || !map(&tdo64, p.dout, 64))
         return FA_ERR_CUDA;
     BwdTcParams k;
     k.lse = p.lse;
@@ -612,6 +659,10 @@ fa_status launch(const FaBwdProblem &p) {
     k.dq = p.dq;
     k.dk = p.dk;
     k.dv = p.dv;
+    k.cu = p.cu_seqlens;
+    k.varlen = p.varlen;
+    k.heads = p.heads;
+    k.total = p.total;
     k.n = p.n;
     k.nblk = (p.n + kT - 1) / kT;
     k.scale = p.scale;

@@ -44,9 +44,14 @@ struct FaBwdProblem {
     const void *q, *k, *v, *o, *dout;
     const float *lse;
     void *dq, *dk, *dv;
-    float *delta;     // [B*H*N] float32 (workspace)
-    int units_bh;     // B*H
-    int n;            // N
+    float *delta;     // float32 workspace, laid out like L
+    const int32_t *cu_seqlens;  // null for a dense batch
+    int varlen;
+    int heads;        // H
+    int num_seqs;     // varlen only
+    int64_t total;    // varlen: total tokens (L / delta are [H, total])
+    int units_bh;     // dense: B*H; varlen: num_seqs*H
+    int n;            // dense: N; varlen: max_seqlen
     int D;
     float scale;
     int causal;

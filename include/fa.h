@@ -254,6 +254,35 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N);
 
 /*
+ * fa_bwd_varlen -- gradients of the packed-batch forward pass
+ * (fa_fwd_varlen): the same operation as fa_bwd for every sequence and
+ * head, with fa_fwd_varlen's layout.
+ *
+ *   Q, K, V, O, dO, dQ, dK, dV : [total_tokens, H, D] contiguous
+ *   L                          : [H, total_tokens] float32
+ *   cu_seqlens, num_seqs, max_seqlen : as fa_fwd_varlen (DEVICE int32
+ *                  offsets, checked on the device; a violation skips the
+ *                  sequence and is reported by fa_check_device_error())
+ *   workspace      : at least fa_bwd_varlen_workspace_size(total_tokens, H)
+ *                    bytes of DEVICE memory, 16-byte aligned (rowsum(dO * O),
+ *                    laid out like L)
+ *
+ * Each sequence's rows and keys are its own: nothing crosses a sequence
+ * boundary, so no buffer needs gaps between sequences.  Other arguments,
+ * types and errors as fa_bwd.
+ */
+FA_API fa_status fa_bwd_varlen(const void *Q, const void *K, const void *V, const void *O,
+                               const void *dO, const float *L, void *dQ, void *dK, void *dV,
+                               const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                               int max_seqlen, int H, int D, float scale, int causal,
+                               fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                               fa_stream_t stream);
+
+/* Workspace bytes fa_bwd_varlen needs: 4 * total_tokens * H rounded up to
+ * 256 (0 for an empty problem or negative sizes). */
+FA_API size_t fa_bwd_varlen_workspace_size(int total_tokens, int H);
+
+/*
  * fa_check_device_error -- synchronise `stream`, then return (and clear)
  * the status recorded by kernels of this library on the current device:
  * FA_ERR_DEVICE_TIMEOUT if a device wait ran out, FA_ERR_INVALID_ARG if a

@@ -218,3 +218,25 @@ def test_bwd_argument_checks(lib):
     if not torch.cuda.is_available():   # valid arguments reach CUDA, which is absent
         assert call() == fa.FA_ERR_CUDA
         assert call(dtype=fa.FA_F32) == fa.FA_ERR_CUDA
+
+
+def test_bwd_varlen_argument_checks(lib):
+    q, k, v, o, do, l, dq, dk, dv, ws = _bwd_ptrs()
+    cu = A + 11 * STEP
+    nws = fa.fa_bwd_varlen_workspace_size(100, 2)
+    assert nws == 1024 and fa.fa_bwd_varlen_workspace_size(0, 2) == 0
+    bad = fa.FA_ERR_INVALID_ARG
+
+    def call(*, c=cu, ns=2, tot=100, mx=50, H=2, D=64, p=None, w=ws, nw=nws):
+        args = list(p or (q, k, v, o, do, l, dq, dk, dv))
+        return fa.fa_bwd_varlen(*args, c, ns, tot, mx, H, D, 0.1, 1, fa.FA_BF16, w, nw, 0)
+
+    assert call(ns=-1) == bad and call(tot=-1) == bad and call(mx=-3) == bad and call(H=-1) == bad
+    assert call(c=0) == bad and call(c=cu + 2) == bad
+    assert call(D=80) == fa.FA_ERR_UNSUPPORTED
+    assert call(w=0) == bad and call(nw=4 * 100 * 2 - 4) == bad   # one float short
+    assert call(p=[q, k, v, o, do, l, q + 64, dk, dv]) == bad
+    assert fa.fa_bwd_varlen(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 2, 64, 0.1, 1, fa.FA_BF16, 0, 0,
+                            0) == fa.FA_OK
+    if not torch.cuda.is_available():
+        assert call() == fa.FA_ERR_CUDA

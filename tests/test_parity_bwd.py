@@ -22,7 +22,8 @@ import exact_attention_24_gb300 as fa
 from exact_attention_24_gb300 import build as fa_build
 from exact_attention_24_gb300.workloads import Workload, make_inputs
 from helpers import half_ulp_bf16, to_f64
-from oracle import attention_bwd_ref, attention_bwd_sampled, attention_ref
+from oracle import (attention_bwd_ref, attention_bwd_ref_varlen, attention_bwd_sampled,
+                    attention_ref, attention_ref_varlen)
 
 pytestmark = pytest.mark.gpu
 
@@ -154,3 +155,67 @@ def test_bwd_full_size_sampled(shape):
         ref = attention_bwd_sampled(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, causal, idx, idx)
         mine = [to_f64(got[0][b, h, idx]), to_f64(got[1][b, h, idx]), to_f64(got[2][b, h, idx])]
         assert_grads(mine, ref, fa.FA_BF16, f"full {shape} b={b} h={h}")
+
+
+# ---------------------------------------------------------------- varlen --
+def _varlen_bwd_inputs(lengths, H, D, causal, seed):
+    w = Workload("vbwd", 0, H, 0, D, "bf16", causal, seed, lengths=tuple(lengths))
+    q, k, v = make_inputs(w)
+    do = make_inputs(Workload("vdO", 0, H, 0, D, "bf16", causal, seed + 50_000,
+                              lengths=tuple(lengths)))[0]
+    o, lse = attention_ref_varlen(q, k, v, w.cu_seqlens, w.scale, causal)
+    return w, q, k, v, do, torch.from_numpy(o).to(q.dtype), torch.from_numpy(lse).float()
+
+
+def run_bwd_varlen(w, q, k, v, o, do, lse, code):
+    odt = torch.bfloat16 if code == fa.FA_BF16 else torch.float32
+    grads = [torch.full(q.shape, float("nan"), dtype=odt, device=q.device) for _ in range(3)]
+    nbytes = fa.fa_bwd_varlen_workspace_size(w.total, w.H)
+    ws = torch.full((max(nbytes, 16) // 4,), float("nan"), dtype=torch.float32, device=q.device)
+    cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32, device=q.device)
+    st = fa.fa_bwd_varlen(q, k, v, o, do, lse, *grads, cu, len(w.lengths), w.total, w.max_seqlen,
+                          w.H, w.D, w.scale, int(w.causal), code, ws, nbytes, None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    return grads
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen_small(kernel, D, causal):
+    lengths = [0, 1, 127, 128, 129, 300, 5, 0, 260]
+    w, q, k, v, do, o, lse = _varlen_bwd_inputs(lengths, 2, D, causal, seed=D + int(causal))
+    ref = attention_bwd_ref_varlen(q, k, v, do, w.cu_seqlens, w.scale, causal)[:3]
+    dev = [x.to(DEV) for x in (q, k, v, o, do, lse)]
+    for code in BF16_CODES:
+        got = run_bwd_varlen(w, *dev, code)
+        assert_grads([to_f64(x) for x in got], ref, code, f"{kernel} varlen D={D} c={causal} dt={code}")
+
+
+def test_bwd_varlen_f32(kernel):
+    lengths = [3, 0, 200, 64]
+    w = Workload("vbwd32", 0, 3, 0, 64, "f32", True, 9, lengths=tuple(lengths))
+    q, k, v = make_inputs(w)
+    do = make_inputs(Workload("vdO32", 0, 3, 0, 64, "f32", True, 99, lengths=tuple(lengths)))[0]
+    o, lse = attention_ref_varlen(q, k, v, w.cu_seqlens, w.scale, True)
+    o, lse = torch.from_numpy(o).float(), torch.from_numpy(lse).float()
+    ref = attention_bwd_ref_varlen(q, k, v, do, w.cu_seqlens, w.scale, True)[:3]
+    got = run_bwd_varlen(w, *[x.to(DEV) for x in (q, k, v, o, do, lse)], fa.FA_F32)
+    assert_grads([to_f64(x) for x in got], ref, fa.FA_F32, f"{kernel} varlen f32")
+
+
+def test_bwd_varlen_full_size_sampled():
+    """The 16-sequence packed workload (lengths uniform in [128, 4096]) in the
+    default kernel selection, on sampled rows and keys of three sequences."""
+    from exact_attention_24_gb300.workloads import C5
+    w, q, k, v, do, o, lse = _varlen_bwd_inputs(C5.lengths, C5.H, C5.D, True, seed=C5.seed)
+    got = run_bwd_varlen(w, *[x.to(DEV) for x in (q, k, v, o, do, lse)], fa.FA_BF16)
+    cu = w.cu_seqlens
+    rng = np.random.default_rng(7)
+    for s, h in [(0, 0), (7, 9), (15, 15)]:
+        a, b = int(cu[s]), int(cu[s + 1])
+        n = b - a
+        idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 12)]))
+        ref = attention_bwd_sampled(q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], w.scale, True, idx, idx)
+        mine = [to_f64(got[0][a + idx, h]), to_f64(got[1][a + idx, h]), to_f64(got[2][a + idx, h])]
+        assert_grads(mine, ref, fa.FA_BF16, f"varlen full s={s} h={h}")
