@@ -72,6 +72,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// 32-byte global store (eight 32-bit words); `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 struct WaitCtx {
     uint32_t *err;               // device error word
     volatile int *abort_flag;    // CTA-wide abort flag in shared memory

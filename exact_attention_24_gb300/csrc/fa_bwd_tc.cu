@@ -126,7 +126,6 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *tm, u
 // half-tile's load is issued two halves before its first MMA.
 template <int D>
 struct DkCfg {
-    static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kT * D * 2;       // K or V (128 rows)
     static constexpr int kHalfBytes = 64 * D * 2;       // Q_x or dO_x (64 rows)
     static constexpr int kHalfAtom = 64 * 128;          // one 64-element-wide box of 64 rows

@@ -110,6 +110,7 @@ struct TcParams {
     int wl, wr;        // key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     uint32_t *err;
     uint64_t wait_limit_ns;
+    int o_v8;          // output base 32-byte aligned: the epilogue stores 32 B per instruction
 };
 
 // One work item = one 256-row block (two query tiles) of one (b, h) or
@@ -817,7 +818,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float o[32];
                 tmem_ld32(t_o + cc * 32, o);
                 tmem_wait_ld();
-                if (store) {
+                if (!WIN && store && p.o_v8) {
+                    // 32-byte stores: every sector a thread touches is written whole
+                    // (measured faster for causal / full attention, slower for the
+                    // short items of a narrow band)
+                    if (OUT != kOutBf16) {
+                        float *dst = o32 + orow + cc * 32;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(o[8 * i + e] * inv);
+                            st_global_v8(dst + 8 * i, w);
+                        }
+                    } else {
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.o) + orow + cc * 32;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                w[e] = pack_bf16x2(o[16 * i + 2 * e] * inv, o[16 * i + 2 * e + 1] * inv);
+                            st_global_v8(dst + 16 * i, w);
+                        }
+                    }
+                } else if (store) {
                     if (OUT != kOutBf16) {
                         float4 *dst = reinterpret_cast<float4 *>(o32 + orow + cc * 32);
 #pragma unroll
@@ -960,6 +985,7 @@ fa_status launch(const FaProblem &pr, int splits) {
     p.wr = pr.wr;
     p.err = pr.err;
     p.wait_limit_ns = pr.wait_limit_ns;
+    p.o_v8 = (reinterpret_cast<uintptr_t>(OUT == kOutPart ? static_cast<void *>(p.ws_o) : p.o) & 31u) == 0;
     int grid = pr.grid_ctas > 0 ? pr.grid_ctas : num_sms();
     if (grid <= 0) return FA_ERR_CUDA;  // device query failed (recorded)
     if (grid > p.num_items) grid = p.num_items;
