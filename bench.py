@@ -353,6 +353,7 @@ def bench_ours(args, w, rank, world, local):
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
         "roofline": roofline,
         "io": {"min_bytes": min_bytes,
+               "achieved_hbm_gbs": round(min_bytes / t_launch / 1e9, 1),
                "tile_model_bytes": io_model_bytes(w, 256, 128),
                "tile_model_bytes_64x64": io_model_bytes(w, 64, 64)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
@@ -540,7 +541,7 @@ def cpu_baseline_bwd(w, seconds: float):
         outs += c
         it += 1
     return {"value": done / t_total / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
+            "kind": "oracle", "host": host_info(),
             "sample": f"{outs} gradient rows and keys ({it} heads x 32 random dQ rows and 32 random "
                       f"dK/dV keys, each head's forward recomputed) of {w.name}, float64 NumPy, "
                       f"{t_total:.1f} s"}
@@ -646,6 +647,22 @@ def _f64_views(w):
     return head_views(w, qf, kf, vf)
 
 
+def host_info() -> dict:
+    """The host the oracle runs on: CPU model and the BLAS thread setting."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and not model:
+                    model = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    threads = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+               if k in os.environ}
+    return {"cpu_model": model or os.uname().machine, "blas_threads": threads or "library default (all cores)"}
+
+
 def cpu_baseline(w, seconds: float, seed: int = 0):
     """Time the oracle as it stands on this host's cores, on a bounded sample
     of the workload's rows (float64; causal rows count only their keys)."""
@@ -663,7 +680,7 @@ def cpu_baseline(w, seconds: float, seed: int = 0):
         it += 1
     cores = len(os.sched_getaffinity(0))
     return {"value": done_flops / t_total / 1e12, "unit": UNIT, "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "host": host_info(),
             "sample": f"{n_rows} query rows ({it} heads x up to {rows} random rows) of {w.name}, "
                       f"float64 NumPy, {t_total:.1f} s"}
 

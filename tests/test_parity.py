@@ -439,3 +439,22 @@ def test_window_argument_checks():
     L = torch.zeros(1, 1, 16, device=DEV)
     assert fa.fa_fwd_window(q, q, q, O, L, 1, 1, 16, 64, 0.1, -2, 0, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_window(q, q, q, O, L, 1, 1, 16, 64, 0.1, 0, -5, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("code", [fa.FA_BF16, fa.FA_BF16_OUT_F32])
+def test_output_only_16_byte_aligned(kernel, code):
+    """The epilogue stores 32 bytes at a time when O is 32-byte aligned and
+    16 bytes otherwise; both give the same bits."""
+    w, q, k, v = _dense_case(1, 2, 700, 128, "bf16", True, seed=44)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    O1, L1 = run_dense(qd, kd, vd, True, code, w.scale)
+    odt = torch.bfloat16 if code == fa.FA_BF16 else torch.float32
+    pad = 16 // torch.tensor([], dtype=odt).element_size()
+    flat = torch.full((O1.numel() + 64,), float("nan"), dtype=odt, device=DEV)
+    base = (-flat.data_ptr() // flat.element_size()) % (32 // flat.element_size())  # 32-aligned start
+    O2 = flat[base + pad: base + pad + O1.numel()].view(O1.shape)
+    assert O2.data_ptr() % 32 == 16
+    L2 = torch.full_like(L1, float("nan"))
+    st = fa.fa_fwd(qd, kd, vd, O2, L2, 1, 2, 700, 128, w.scale, 1, code, None)
+    assert st == fa.FA_OK and fa.fa_check_device_error(None) == fa.FA_OK
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
