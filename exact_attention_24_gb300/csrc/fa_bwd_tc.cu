@@ -44,6 +44,7 @@ struct BwdTcParams {
     const int32_t *cu;    // packed batch: sequence offsets (null for dense)
     int varlen, heads;
     int64_t total;
+    int units;            // problems: B*H, or num_seqs*H
     int n, nblk;          // n: N, or the longest sequence of a packed batch
     float scale, scale_log2;
     int causal;
@@ -138,15 +139,39 @@ struct DkCfg {
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(8 * (1 + 2 * kSlots + 6) + 16 <= kBarBytes, "barrier area");
+    static_assert(8 * (2 + 2 * kSlots + 7) + 16 <= kBarBytes, "barrier area");
 };
 
+// K/V loaded and free again, ring full/empty per slot, S^T/dP^T ready and
+// P^T/dS^T ready per half-buffer, accumulators final and read, drain.
 struct DkBars {
-    uint32_t fix_full, ring_full, ring_empty, s_full, p_full, o_final, drain;
+    uint32_t fix_full, kv_free, ring_full, ring_empty, s_full, p_full, o_final, acc_free, drain;
     __device__ DkBars(uint32_t b, int slots)
-        : fix_full(b), ring_full(b + 8), ring_empty(b + 8 + 8 * slots), s_full(b + 8 + 16 * slots),
-          p_full(b + 24 + 16 * slots), o_final(b + 40 + 16 * slots), drain(b + 48 + 16 * slots) {}
+        : fix_full(b), kv_free(b + 8), ring_full(b + 16), ring_empty(b + 16 + 8 * slots),
+          s_full(b + 16 + 16 * slots), p_full(b + 32 + 16 * slots), o_final(b + 48 + 16 * slots),
+          acc_free(b + 56 + 16 * slots), drain(b + 64 + 16 * slots) {}
 };
+
+// The CTA's next dK/dV work item at or after walk position k: items are
+// numbered key block first (lowest first: under the causal mask it has the
+// most query rows), then problem; CTA c takes items c, 2G-1-c, 2G+c, ...
+// Blocks past the end of their sequence are skipped.
+__device__ __forceinline__ bool next_dk_item(const BwdTcParams &p, int &k, int cta, int G, int D, Seq &sq,
+                                             int &j0) {
+    const int items = p.nblk * p.units;
+    for (; k * G < items; ++k) {
+        const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+        if (idx >= items) continue;
+        const int jb = idx / p.units, unit = idx % p.units;
+        sq = seq_of(p, unit, D);
+        j0 = jb * kT;
+        if (j0 < sq.len) {
+            ++k;
+            return true;
+        }
+    }
+    return false;
+}
 
 // S^T_x (TMEM, 128 keys x 64 queries fp32) = K (smem, 128 x D) * Q_x^T
 // (smem, 64 x D): both K-major; K's 64-element boxes are 16 KB apart, a
@@ -179,6 +204,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdTcParams p) {
+    // Persistent: each CTA walks its items in turn.  Across an item boundary
+    // K and V are reloaded as soon as the item's last S^T, dP^T have been
+    // issued, and the next item's first S^T, dP^T run while the softmax
+    // warps store the previous dK, dV; its first accumulating MMA waits until
+    // they have read them (acc_free).  Barrier phases and ring slots count
+    // halves and items over the CTA's whole walk.
     using C = DkCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -189,17 +220,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
     float *stat = reinterpret_cast<float *>(gbase + C::kStatOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int unit = blockIdx.x / p.nblk, jb = blockIdx.x % p.nblk;  // lowest key block first
-    const int j0 = jb * kT;
-    const Seq sq = seq_of(p, unit, D);
-    if (j0 >= sq.len) return;  // block past the end of this sequence (packed batch)
-    const int n = sq.len;
-    const int i_first = p.causal ? j0 : 0;
-    const int halves = 2 * ((n - i_first + kT - 1) / kT);
+    const int cta = blockIdx.x, G = gridDim.x;
 
     if (warp == kProdWarp && lane == 0) {
         mbar_init(b.fix_full, 1);
+        mbar_init(b.kv_free, 1);
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(b.ring_full + 8 * i, 1);
             mbar_init(b.ring_empty + 8 * i, 1);
@@ -209,6 +234,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b.p_full + 8 * x, 4);
         }
         mbar_init(b.o_final, 1);
+        mbar_init(b.acc_free, 4);
         mbar_init(b.drain, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -231,21 +257,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kProdWarp) {
         // ---------------------------------------------------- producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
-            load_rows<D>(base, &tm_k, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
-            load_rows<D>(base + C::kTileBytes, &tm_v, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
-            int u = 0;
-            for (; u < halves; ++u) {
-                const int slot = u % C::kSlots, round = u / C::kSlots;
-                if (round > 0 && !mbar_wait(b.ring_empty + 8 * slot, (round - 1) & 1, wc, 0x41)) break;
-                const uint32_t dst = ring + slot * C::kSlotBytes, fb = b.ring_full + 8 * slot;
-                mbar_arrive_expect_tx(fb, C::kSlotBytes);
-                load_rows<D>(dst, &tm_q, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
-                load_rows<D>(dst + C::kHalfBytes, &tm_do, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
+            int k = 0, it = 0, g = 0;  // walk position, items, halves loaded
+            bool ok = true;
+            Seq sq;
+            int j0;
+            while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+                const int i_first = p.causal ? j0 : 0;
+                const int halves = 2 * ((sq.len - i_first + kT - 1) / kT);
+                if (it > 0 && !mbar_wait(b.kv_free, (it - 1) & 1, wc, 0x40)) break;
+                mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
+                load_rows<D>(base, &tm_k, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
+                load_rows<D>(base + C::kTileBytes, &tm_v, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
+                ++it;
+                for (int u = 0; u < halves; ++u, ++g) {
+                    const int slot = g % C::kSlots, round = g / C::kSlots;
+                    if (round > 0 && !mbar_wait(b.ring_empty + 8 * slot, (round - 1) & 1, wc, 0x41)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = ring + slot * C::kSlotBytes, fb = b.ring_full + 8 * slot;
+                    mbar_arrive_expect_tx(fb, C::kSlotBytes);
+                    load_rows<D>(dst, &tm_q, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
+                    load_rows<D>(dst + C::kHalfBytes, &tm_do, fb, i_first + 64 * u, sq, p.varlen, C::kHalfAtom);
+                }
             }
             const uint64_t lim = p.wait_limit_ns;
-            mbar_drain(b.fix_full, 0, lim);
-            for (int v = u > C::kSlots ? u - C::kSlots : 0; v < u; ++v)
+            if (it > 0) mbar_drain(b.fix_full, (it - 1) & 1, lim);
+            for (int v = g > C::kSlots ? g - C::kSlots : 0; v < g; ++v)
                 mbar_drain(b.ring_full + 8 * (v % C::kSlots), (v / C::kSlots) & 1, lim);
         }
     } else if (warp == kMmaWarp) {
@@ -256,46 +294,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t d_ring_k = smem_desc(ring, 16, 1024);                 // K-major view
         const uint64_t d_ring_mn = smem_desc(ring, C::kHalfAtom, 1024);      // MN-major view
         const uint32_t t_dv = tmem + 2 * kT, t_dk = t_dv + D;
-        bool ok = warp_wait(b.fix_full, 0, wc, 0x50);
-        // S^T_x, dP^T_x of half u (buffer x = u & 1) from its ring slot
-        for (int u = 0; ok && u < 2 && u < halves; ++u) {
-            if (!ring_wait(b.ring_full, u, C::kSlots, wc, 0x51)) { ok = false; break; }
-            tc_fence_after();
-            if (elect_one()) {
-                const uint64_t sl = (u % C::kSlots) * kSlotDesc;
-                const uint32_t t_st = tmem + u * 2 * 64;
-                issue_st_half<D>(t_st, d_k, d_ring_k + sl);
-                issue_st_half<D>(t_st + 64, d_v, d_ring_k + sl + kHalfDesc);
-                mma_commit(b.s_full + 8 * u);
-            }
-            __syncwarp();
-        }
-        for (int u = 0; ok && u < halves; ++u) {
-            const int x = u & 1;
-            const uint32_t t_st = tmem + x * 2 * 64, t_dpt = t_st + 64;
-            if (!warp_wait(b.p_full + 8 * x, (u >> 1) & 1, wc, 0x52)) break;
-            const bool next = u + 2 < halves;
-            if (next && !ring_wait(b.ring_full, u + 2, C::kSlots, wc, 0x53)) break;
-            tc_fence_after();
-            if (elect_one()) {
-                const uint64_t sl = (u % C::kSlots) * kSlotDesc;
-                const uint32_t acc = u > 0 ? 1u : 0u;
-                issue_acc_half<D>(t_dv, t_st, d_ring_mn + sl + kHalfDesc, acc);   // dV += P^T dO_x
-                issue_acc_half<D>(t_dk, t_dpt, d_ring_mn + sl, acc);              // dK += dS^T Q_x
-                mma_commit(b.ring_empty + 8 * (u % C::kSlots));
-                if (next) {
-                    const uint64_t sn = ((u + 2) % C::kSlots) * kSlotDesc;
-                    issue_st_half<D>(t_st, d_k, d_ring_k + sn);
-                    issue_st_half<D>(t_dpt, d_v, d_ring_k + sn + kHalfDesc);
-                    mma_commit(b.s_full + 8 * x);
+        int k = 0, it = 0, g = 0;
+        bool ok = true;
+        Seq sq;
+        int j0;
+        while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+            const int i_first = p.causal ? j0 : 0;
+            const int halves = 2 * ((sq.len - i_first + kT - 1) / kT);
+            if (!warp_wait(b.fix_full, it & 1, wc, 0x50)) break;
+            // S^T_x, dP^T_x of the item's first two halves (buffer x = half & 1)
+            for (int u = 0; u < 2 && u < halves; ++u) {
+                if (!ring_wait(b.ring_full, g + u, C::kSlots, wc, 0x51)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint64_t sl = ((g + u) % C::kSlots) * kSlotDesc;
+                    const uint32_t t_st = tmem + u * 2 * 64;
+                    issue_st_half<D>(t_st, d_k, d_ring_k + sl);
+                    issue_st_half<D>(t_st + 64, d_v, d_ring_k + sl + kHalfDesc);
+                    mma_commit(b.s_full + 8 * u);
                 }
+                __syncwarp();
             }
+            if (!ok) break;
+            if (halves <= 2) {                          // K and V have had their last reader
+                if (elect_one()) mma_commit(b.kv_free);
+                __syncwarp();
+            }
+            // the previous item's dK, dV have been read out of TMEM
+            if (it > 0 && !warp_wait(b.acc_free, (it - 1) & 1, wc, 0x59)) break;
+            for (int u = 0; u < halves; ++u) {
+                const int gu = g + u, x = u & 1;
+                const uint32_t t_st = tmem + x * 2 * 64, t_dpt = t_st + 64;
+                if (!warp_wait(b.p_full + 8 * x, (gu >> 1) & 1, wc, 0x52)) { ok = false; break; }
+                const bool next = u + 2 < halves;
+                if (next && !ring_wait(b.ring_full, gu + 2, C::kSlots, wc, 0x53)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint64_t sl = (gu % C::kSlots) * kSlotDesc;
+                    const uint32_t acc = u > 0 ? 1u : 0u;
+                    issue_acc_half<D>(t_dv, t_st, d_ring_mn + sl + kHalfDesc, acc);   // dV += P^T dO_x
+                    issue_acc_half<D>(t_dk, t_dpt, d_ring_mn + sl, acc);              // dK += dS^T Q_x
+                    mma_commit(b.ring_empty + 8 * (gu % C::kSlots));
+                    if (next) {
+                        const uint64_t sn = ((gu + 2) % C::kSlots) * kSlotDesc;
+                        issue_st_half<D>(t_st, d_k, d_ring_k + sn);
+                        issue_st_half<D>(t_dpt, d_v, d_ring_k + sn + kHalfDesc);
+                        mma_commit(b.s_full + 8 * x);
+                        if (u + 2 == halves - 1) mma_commit(b.kv_free);   // last reader of K, V
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (elect_one()) mma_commit(b.o_final);
             __syncwarp();
+            g += halves;
+            ++it;
         }
-        if (elect_one()) {
-            mma_commit(b.o_final);
-            mma_commit(b.drain);
-        }
+        if (elect_one()) mma_commit(b.drain);
         __syncwarp();
         mbar_drain(b.drain, 0, p.wait_limit_ns);
     } else {
@@ -305,77 +361,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t t_s = tmem + lane_off;
         const uint32_t t_dv = t_s + 2 * kT, t_dk = t_dv + D;
         const float c = p.scale_log2;
-        const float *L = p.lse + sq.stat0;
-        const float *Dl = p.delta + sq.stat0;
-        // threads 0..63 stage the row statistics of query r of each half,
-        // loaded one half ahead
-        int iq = i_first + r;
-        float nl = 0.f, nd = 0.f;
-        if (r < 64) {
-            nl = iq < n ? L[iq] * kLog2e : INFINITY;
-            nd = iq < n ? Dl[iq] : 0.f;
-        }
+        int k = 0, it = 0, g = 0;
         bool ok = true;
-        for (int u = 0; u < halves; ++u) {
-            const int x = u & 1;
-            float *sl = stat + x * 2 * 64, *sd = sl + 64;
+        Seq sq;
+        int j0;
+        while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+            const int n = sq.len;
+            const int i_first = p.causal ? j0 : 0;
+            const int halves = 2 * ((n - i_first + kT - 1) / kT);
+            const float *L = p.lse + sq.stat0;
+            const float *Dl = p.delta + sq.stat0;
+            // threads 0..63 stage the row statistics of query r of each half,
+            // loaded one half ahead
+            int iq = i_first + r;
+            float nl = 0.f, nd = 0.f;
             if (r < 64) {
-                sl[r] = nl;
-                sd[r] = nd;
-                iq += 64;
-                if (u + 1 < halves) {
-                    nl = iq < n ? L[iq] * kLog2e : INFINITY;
-                    nd = iq < n ? Dl[iq] : 0.f;
-                }
+                nl = iq < n ? L[iq] * kLog2e : INFINITY;
+                nd = iq < n ? Dl[iq] : 0.f;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            const uint32_t t_st = t_s + x * 2 * 64, t_dpt = t_st + 64;
-            if (!warp_wait(b.s_full + 8 * x, (u >> 1) & 1, wc, 0x60)) { ok = false; break; }
-            tc_fence_after();
-            // causal: query q sees key r iff q >= r; only the first tile holds
-            // queries below some key of the block
-            const bool diag = p.causal && u < 2;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                float sv[32], dpv[32];
-                tmem_ld32(t_st + cc * 32, sv);
-                tmem_ld32(t_dpt + cc * 32, dpv);
-                tmem_wait_ld();
-                uint32_t pk[16], dk[16];
-                const float2 c2 = make_float2(c, c);
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int qi = cc * 32 + e;              // query within the half
-                    // the statistics of four queries: one 16-byte broadcast load each
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + qi);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + qi);
-                    const float2 a0 = __ffma2_rn(make_float2(sv[e], sv[e + 1]), c2, make_float2(-l4.x, -l4.y));
-                    const float2 a1 = __ffma2_rn(make_float2(sv[e + 2], sv[e + 3]), c2, make_float2(-l4.z, -l4.w));
-                    float2 p0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
-                    float2 p1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
-                    if (diag) {
-                        const int q = x * 64 + qi;
-                        if (q < r) p0.x = 0.f;
-                        if (q + 1 < r) p0.y = 0.f;
-                        if (q + 2 < r) p1.x = 0.f;
-                        if (q + 3 < r) p1.y = 0.f;
+            for (int u = 0; u < halves; ++u) {
+                const int gu = g + u, x = u & 1;
+                float *sl = stat + x * 2 * 64, *sd = sl + 64;
+                if (r < 64) {
+                    sl[r] = nl;
+                    sd[r] = nd;
+                    iq += 64;
+                    if (u + 1 < halves) {
+                        nl = iq < n ? L[iq] * kLog2e : INFINITY;
+                        nd = iq < n ? Dl[iq] : 0.f;
                     }
-                    const float2 g0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dpv[e], dpv[e + 1]), make_float2(-d4.x, -d4.y)));
-                    const float2 g1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dpv[e + 2], dpv[e + 3]), make_float2(-d4.z, -d4.w)));
-                    pk[e / 2] = pack_bf16x2(p0.x, p0.y);
-                    pk[e / 2 + 1] = pack_bf16x2(p1.x, p1.y);
-                    dk[e / 2] = pack_bf16x2(g0.x, g0.y);
-                    dk[e / 2 + 1] = pack_bf16x2(g1.x, g1.y);
                 }
-                tmem_st16(t_st + cc * 16, pk);    // P^T over S^T columns already read
-                tmem_st16(t_dpt + cc * 16, dk);   // dS^T over dP^T columns already read
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                const uint32_t t_st = t_s + x * 2 * 64, t_dpt = t_st + 64;
+                if (!warp_wait(b.s_full + 8 * x, (gu >> 1) & 1, wc, 0x60)) { ok = false; break; }
+                tc_fence_after();
+                // causal: query q sees key r iff q >= r; only the first tile holds
+                // queries below some key of the block
+                const bool diag = p.causal && u < 2;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float sv[32], dpv[32];
+                    tmem_ld32(t_st + cc * 32, sv);
+                    tmem_ld32(t_dpt + cc * 32, dpv);
+                    tmem_wait_ld();
+                    uint32_t pk[16], dk[16];
+                    const float2 c2 = make_float2(c, c);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const int qi = cc * 32 + e;              // query within the half
+                        // the statistics of four queries: one 16-byte broadcast load each
+                        const float4 l4 = *reinterpret_cast<const float4 *>(sl + qi);
+                        const float4 d4 = *reinterpret_cast<const float4 *>(sd + qi);
+                        const float2 a0 = __ffma2_rn(make_float2(sv[e], sv[e + 1]), c2, make_float2(-l4.x, -l4.y));
+                        const float2 a1 = __ffma2_rn(make_float2(sv[e + 2], sv[e + 3]), c2, make_float2(-l4.z, -l4.w));
+                        float2 p0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+                        float2 p1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
+                        if (diag) {
+                            const int q = x * 64 + qi;
+                            if (q < r) p0.x = 0.f;
+                            if (q + 1 < r) p0.y = 0.f;
+                            if (q + 2 < r) p1.x = 0.f;
+                            if (q + 3 < r) p1.y = 0.f;
+                        }
+                        const float2 g0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dpv[e], dpv[e + 1]), make_float2(-d4.x, -d4.y)));
+                        const float2 g1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dpv[e + 2], dpv[e + 3]), make_float2(-d4.z, -d4.w)));
+                        pk[e / 2] = pack_bf16x2(p0.x, p0.y);
+                        pk[e / 2 + 1] = pack_bf16x2(p1.x, p1.y);
+                        dk[e / 2] = pack_bf16x2(g0.x, g0.y);
+                        dk[e / 2 + 1] = pack_bf16x2(g1.x, g1.y);
+                    }
+                    tmem_st16(t_st + cc * 16, pk);    // P^T over S^T columns already read
+                    tmem_st16(t_dpt + cc * 16, dk);   // dS^T over dP^T columns already read
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b.p_full + 8 * x);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b.p_full + 8 * x);
-        }
-        if (ok && warp_wait(b.o_final, 0, wc, 0x61)) {
+            if (!ok) break;
+            if (!warp_wait(b.o_final, it & 1, wc, 0x61)) break;
             tc_fence_after();
             const int key = j0 + r;
             Tout *dV = static_cast<Tout *>(p.dv) + sq.elem0 + key * sq.rstride;
@@ -390,6 +454,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 if (key < n) store_row(dK + cc * 32, xo, p.scale);
             }
+            // dK, dV are out of TMEM: the next item may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.acc_free);
+            g += halves;
+            ++it;
         }
     }
     tc_fence_before();
@@ -659,6 +729,7 @@ fa_status launch(const FaBwdProblem &p) {
     k.dk = p.dk;
     k.dv = p.dv;
     k.cu = p.cu_seqlens;
+    k.units = p.units_bh;
     k.varlen = p.varlen;
     k.heads = p.heads;
     k.total = p.total;
@@ -678,8 +749,11 @@ fa_status launch(const FaBwdProblem &p) {
         if (st != FA_OK) return st;
         ready = true;
     }
-    bwd_dkdv_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv,
-                                                                                           tdo64, k);
+    int grid_dk = p.grid_ctas > 0 ? p.grid_ctas : num_sms();   // persistent: one CTA per SM
+    if (grid_dk <= 0) return FA_ERR_CUDA;
+    if (grid_dk > grid) grid_dk = (int)grid;
+    bwd_dkdv_tc_kernel<D, Tout><<<grid_dk, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv, tdo64,
+                                                                                         k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
     bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
