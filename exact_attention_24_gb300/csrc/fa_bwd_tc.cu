@@ -480,7 +480,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //   dQ += dS_t K_t
 //   S_{t+2} = Q K_{t+2}^T     (into dS_t's buffer, after dQ read it)
 // so the softmax warps' next input (S_{t+1}, computed a tile earlier, and
-// dP_{t+1}) waits for one MMA only.
+// dP_{t+1}) waits for one MMA only.  Persistent like the dK/dV kernel: Q
+// and dO are reloaded once the item's last dP is issued, the next item's
+// first S, dP run during the previous epilogue, and its first dQ MMA waits
+// for that epilogue to have read dQ.
 template <int D>
 struct DqCfg {
     static constexpr int kTileBytes = kT * D * 2;
@@ -490,9 +493,32 @@ struct DqCfg {
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(8 * (1 + 2 * kSlots + 4) + 16 <= kBarBytes, "barrier area");
+    static_assert(8 * (2 + 2 * kSlots + 5) + 16 <= kBarBytes, "barrier area");
     static_assert(3 * kT + D <= (int)kTmemCols, "TMEM columns");
 };
+
+// The CTA's next dQ work item: query block first (highest first: under the
+// causal mask it has the most keys), then problem; snake over CTAs.
+__device__ __forceinline__ bool next_dq_item(const BwdTcParams &p, int &k, int cta, int G, int D, Seq &sq,
+                                             int &ib) {
+    const int items = p.nblk * p.units;
+    for (; k * G < items; ++k) {
+        const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+        if (idx >= items) continue;
+        ib = p.nblk - 1 - idx / p.units;
+        sq = seq_of(p, idx % p.units, D);
+        if (ib * kT < sq.len) {
+            ++k;
+            return true;
+        }
+    }
+    return false;
+}
+
+__device__ __forceinline__ int dq_tiles(const BwdTcParams &p, int ib, int len) {
+    const int key_tiles = (len + kT - 1) / kT;
+    return p.causal ? min(ib + 1, key_tiles) : key_tiles;
+}
 
 template <int D, typename Tout>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -505,24 +531,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t bars = base + C::kBarOff;
-    const uint32_t fix_full = bars, kv_full = bars + 8, kv_empty = kv_full + 8 * C::kSlots;
+    const uint32_t fix_full = bars, qd_free = bars + 8, kv_full = bars + 16, kv_empty = kv_full + 8 * C::kSlots;
     const uint32_t s_full = kv_empty + 8 * C::kSlots, ds_full = s_full + 8, o_final = ds_full + 8;
-    const uint32_t drain = o_final + 8;
+    const uint32_t acc_free = o_final + 8, drain = acc_free + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int unit = blockIdx.x / p.nblk;
-    const int ib = p.nblk - 1 - blockIdx.x % p.nblk;  // highest query block first
-    const int i0 = ib * kT;
-    const Seq sq = seq_of(p, unit, D);
-    if (i0 >= sq.len) return;  // block past the end of this sequence (packed batch)
-    const int n = sq.len;
-    const int key_tiles = (n + kT - 1) / kT;
-    const int tiles = p.causal ? min(ib + 1, key_tiles) : key_tiles;
+    const int cta = blockIdx.x, G = gridDim.x;
 
     if (warp == kProdWarp && lane == 0) {
         mbar_init(fix_full, 1);
+        mbar_init(qd_free, 1);
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(kv_full + 8 * i, 1);
             mbar_init(kv_empty + 8 * i, 1);
@@ -530,6 +549,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(s_full, 1);
         mbar_init(ds_full, 4);
         mbar_init(o_final, 1);
+        mbar_init(acc_free, 4);
         mbar_init(drain, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -552,25 +572,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kProdWarp) {
         // ---------------------------------------------------- producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
-            load_rows<D>(base, &tm_q, fix_full, i0, sq, p.varlen, kTcAtomBytes);
-            load_rows<D>(base + C::kTileBytes, &tm_do, fix_full, i0, sq, p.varlen, kTcAtomBytes);
-            uint32_t li = 0;
+            int k = 0, it = 0, ib;
+            uint32_t li = 0;          // ring loads issued
             bool ok = true;
-            for (int j = 0; ok && j < tiles; ++j) {
-                for (int kv = 0; kv < 2; ++kv, ++li) {
-                    const uint32_t slot = li % C::kSlots, round = li / C::kSlots;
-                    if (round > 0 && !mbar_wait(kv_empty + 8 * slot, (round - 1) & 1, wc, 0x42)) {
-                        ok = false;
-                        break;
+            Seq sq;
+            while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+                const int tiles = dq_tiles(p, ib, sq.len);
+                if (it > 0 && !mbar_wait(qd_free, (it - 1) & 1, wc, 0x43)) break;
+                mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
+                load_rows<D>(base, &tm_q, fix_full, ib * kT, sq, p.varlen, kTcAtomBytes);
+                load_rows<D>(base + C::kTileBytes, &tm_do, fix_full, ib * kT, sq, p.varlen, kTcAtomBytes);
+                ++it;
+                for (int j = 0; ok && j < tiles; ++j) {
+                    for (int kv = 0; kv < 2; ++kv, ++li) {
+                        const uint32_t slot = li % C::kSlots, round = li / C::kSlots;
+                        if (round > 0 && !mbar_wait(kv_empty + 8 * slot, (round - 1) & 1, wc, 0x42)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
+                        load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
+                                     j * kT, sq, p.varlen, kTcAtomBytes);
                     }
-                    mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
-                    load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
-                                 j * kT, sq, p.varlen, kTcAtomBytes);
                 }
             }
             const uint64_t lim = p.wait_limit_ns;
-            mbar_drain(fix_full, 0, lim);
+            if (it > 0) mbar_drain(fix_full, (it - 1) & 1, lim);
             for (uint32_t u = li > (uint32_t)C::kSlots ? li - C::kSlots : 0; u < li; ++u)
                 mbar_drain(kv_full + 8 * (u % C::kSlots), (u / C::kSlots) & 1, lim);
         }
@@ -581,103 +608,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t d_ring_k = smem_desc(ring, 16, 1024);
         const uint64_t d_ring_mn = smem_desc(ring, kTcAtomBytes, 1024);
         const uint32_t t_dp = tmem + 2 * kT, t_dq = tmem + 3 * kT;
-        // K_j is ring load 2j, V_j load 2j + 1
-        bool ok = warp_wait(fix_full, 0, wc, 0x54) && ring_wait(kv_full, 0, C::kSlots, wc, 0x55) &&
-                  ring_wait(kv_full, 1, C::kSlots, wc, 0x55);
-        if (ok) {
+        int k = 0, it = 0, ib;
+        uint32_t lb = 0, gt = 0;      // ring loads and tiles of earlier items
+        bool ok = true;
+        Seq sq;
+        while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+            const int tiles = dq_tiles(p, ib, sq.len);
+            // K_j is ring load lb + 2j, V_j load lb + 2j + 1; tile t uses S buffer (gt + t) & 1
+            if (!warp_wait(fix_full, it & 1, wc, 0x54) || !ring_wait(kv_full, lb, C::kSlots, wc, 0x55) ||
+                !ring_wait(kv_full, lb + 1, C::kSlots, wc, 0x55))
+                break;
             tc_fence_after();
             if (elect_one()) {
-                issue_qk<D>(tmem, d_q, d_ring_k);                                  // S_0
-                issue_qk<D>(t_dp, d_do, d_ring_k + 1 * kTileDesc);                 // dP_0
+                issue_qk<D>(tmem + (gt & 1) * kT, d_q, d_ring_k + (lb % C::kSlots) * kTileDesc);   // S_0
+                issue_qk<D>(t_dp, d_do, d_ring_k + ((lb + 1) % C::kSlots) * kTileDesc);            // dP_0
                 mma_commit(s_full);
-                mma_commit(kv_empty + 8 * 1);                                      // V_0 read
+                mma_commit(kv_empty + 8 * ((lb + 1) % C::kSlots));                                // V_0 read
+                if (tiles == 1) mma_commit(qd_free);                                            // Q, dO read
             }
             __syncwarp();
-        }
-        if (ok && tiles > 1) {
-            ok = ring_wait(kv_full, 2, C::kSlots, wc, 0x55);
-            if (ok) {
+            if (tiles > 1) {
+                if (!ring_wait(kv_full, lb + 2, C::kSlots, wc, 0x55)) break;
                 tc_fence_after();
-                if (elect_one()) issue_qk<D>(tmem + kT, d_q, d_ring_k + (2 % C::kSlots) * kTileDesc);  // S_1
+                if (elect_one())
+                    issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + ((lb + 2) % C::kSlots) * kTileDesc);
                 __syncwarp();
             }
-        }
-        for (int t = 0; ok && t < tiles; ++t) {
-            const uint32_t t_buf = tmem + (t & 1) * kT;
-            if (!warp_wait(ds_full, t & 1, wc, 0x56)) break;
-            const uint32_t lk = 2 * t, lvn = 2 * t + 3, lk2 = 2 * t + 4;
-            if (t + 1 < tiles && !ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) break;
-            tc_fence_after();
-            if (elect_one()) {
-                if (t + 1 < tiles) {
-                    issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
-                    mma_commit(s_full);
-                    mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+            for (int t = 0; t < tiles; ++t) {
+                const uint32_t g = gt + t;
+                const uint32_t t_buf = tmem + (g & 1) * kT;
+                if (!warp_wait(ds_full, g & 1, wc, 0x56)) { ok = false; break; }
+                const uint32_t lk = lb + 2 * t, lvn = lk + 3, lk2 = lk + 4;
+                if (t + 1 < tiles && !ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) { ok = false; break; }
+                // the previous item's dQ has been read out of TMEM
+                if (t == 0 && it > 0 && !warp_wait(acc_free, (it - 1) & 1, wc, 0x5a)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    if (t + 1 < tiles) {
+                        issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
+                        mma_commit(s_full);
+                        mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+                        if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
+                    }
+                    issue_pv<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
+                    mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
                 }
-                issue_pv<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
-                mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
-            }
-            __syncwarp();
-            if (t + 2 < tiles) {
-                if (!ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) break;
-                tc_fence_after();
-                if (elect_one()) issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
                 __syncwarp();
+                if (t + 2 < tiles) {
+                    if (!ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
+                    __syncwarp();
+                }
             }
+            if (!ok) break;
+            if (elect_one()) mma_commit(o_final);
+            __syncwarp();
+            lb += 2 * tiles;
+            gt += tiles;
+            ++it;
         }
-        if (elect_one()) {
-            mma_commit(o_final);
-            mma_commit(drain);
-        }
+        if (elect_one()) mma_commit(drain);
         __syncwarp();
         mbar_drain(drain, 0, p.wait_limit_ns);
     } else {
         // ------------------------------------------------------- dS
         const int r = warp * 32 + lane;           // query row within the block (TMEM lane)
-        const int row = i0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t t_s0 = tmem + lane_off, t_dp = t_s0 + 2 * kT, t_dq = t_s0 + 3 * kT;
         const float c = p.scale_log2;
-        const float lrow = row < n ? p.lse[sq.stat0 + row] * kLog2e : INFINITY;
-        const float drow = row < n ? p.delta[sq.stat0 + row] : 0.f;
+        int k = 0, it = 0, ib;
+        uint32_t gt = 0;
         bool ok = true;
-        for (int t = 0; t < tiles; ++t) {
-            const uint32_t t_s = t_s0 + (t & 1) * kT;
-            if (!warp_wait(s_full, t & 1, wc, 0x70)) { ok = false; break; }
-            tc_fence_after();
-            const int key0 = t * kT;
+        Seq sq;
+        while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+            const int n = sq.len;
+            const int tiles = dq_tiles(p, ib, n);
+            const int row = ib * kT + r;
+            const float lrow = row < n ? p.lse[sq.stat0 + row] * kLog2e : INFINITY;
+            const float drow = row < n ? p.delta[sq.stat0 + row] : 0.f;
             // keys past the causal diagonal or past the end are masked
             const int lim = p.causal ? min(row + 1, n) : n;
-            const bool need_mask = key0 + kT > lim;
+            for (int t = 0; t < tiles; ++t) {
+                const uint32_t g = gt + t;
+                const uint32_t t_s = t_s0 + (g & 1) * kT;
+                if (!warp_wait(s_full, g & 1, wc, 0x70)) { ok = false; break; }
+                tc_fence_after();
+                const int key0 = t * kT;
+                const bool need_mask = key0 + kT > lim;
 #pragma unroll
-            for (int cc = 0; cc < kT / 32; ++cc) {
-                float sv[32], dpv[32];
-                tmem_ld32(t_s + cc * 32, sv);
-                tmem_ld32(t_dp + cc * 32, dpv);
-                tmem_wait_ld();
-                uint32_t dk[16];
-                const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
-                const float2 nd2 = make_float2(-drow, -drow);
+                for (int cc = 0; cc < kT / 32; ++cc) {
+                    float sv[32], dpv[32];
+                    tmem_ld32(t_s + cc * 32, sv);
+                    tmem_ld32(t_dp + cc * 32, dpv);
+                    tmem_wait_ld();
+                    uint32_t dk[16];
+                    const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
+                    const float2 nd2 = make_float2(-drow, -drow);
 #pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), c2, nl2);
-                    float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-                    if (need_mask) {
-                        const int key = key0 + cc * 32 + x;
-                        if (key >= lim) pp.x = 0.f;
-                        if (key + 1 >= lim) pp.y = 0.f;
+                    for (int x = 0; x < 32; x += 2) {
+                        const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), c2, nl2);
+                        float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                        if (need_mask) {
+                            const int key = key0 + cc * 32 + x;
+                            if (key >= lim) pp.x = 0.f;
+                            if (key + 1 >= lim) pp.y = 0.f;
+                        }
+                        const float2 gg = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
+                        dk[x / 2] = pack_bf16x2(gg.x, gg.y);
                     }
-                    const float2 g = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
-                    dk[x / 2] = pack_bf16x2(g.x, g.y);
+                    tmem_st16(t_s + cc * 16, dk);    // dS over S columns already read
                 }
-                tmem_st16(t_s + cc * 16, dk);    // dS over S columns already read
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ds_full);
-        }
-        if (ok && warp_wait(o_final, 0, wc, 0x71)) {
+            if (!ok) break;
+            if (!warp_wait(o_final, it & 1, wc, 0x71)) break;
             tc_fence_after();
             Tout *dQ = static_cast<Tout *>(p.dq) + sq.elem0 + row * sq.rstride;
 #pragma unroll
@@ -687,6 +735,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 if (row < n) store_row(dQ + cc * 32, x, p.scale);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free);
+            gt += tiles;
+            ++it;
         }
     }
     tc_fence_before();
@@ -756,7 +809,7 @@ fa_status launch(const FaBwdProblem &p) {
                                                                                          k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    bwd_dq_tc_kernel<D, Tout><<<(int)grid, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    bwd_dq_tc_kernel<D, Tout><<<grid_dk, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
     e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
