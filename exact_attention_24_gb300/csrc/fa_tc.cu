@@ -62,6 +62,9 @@ constexpr int kOutPart = 2;   // split-key partial: O_g fp32 and L_g into the wo
 // Varlen batches with at most kMaxSchedSeqs sequences and kMaxSchedLevels
 // 256-row blocks per sequence get a compact schedule (see decode_item).
 constexpr int kMaxSchedSeqs = 384;
+// K/V bytes of the heads that a varlen batch's compact order keeps in
+// flight together (the L2 is 129 MB; Q, O and other traffic share it).
+constexpr double kL2GroupBytes = 64.0 * 1024 * 1024;
 constexpr int kMaxSchedLevels = 128;
 
 template <int D>
@@ -80,7 +83,7 @@ struct Cfg {
     static constexpr bool kPAlias = (D == 128);
     static constexpr int kBarBytes = kPAlias ? 256 : 512;
     static constexpr int kSchedOff = kBarOff + kBarBytes;         // varlen schedule table
-    static constexpr int kSchedBytes = 2 * (kMaxSchedSeqs + kMaxSchedLevels);
+    static constexpr int kSchedBytes = 2 * (kMaxSchedSeqs + kMaxSchedLevels) + 16;
     static constexpr int kSmemBytes = kSchedOff + kSchedBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     // q full/empty, ring full/empty, s_full, p_full, o_final, s_free, pv_done
@@ -102,6 +105,7 @@ struct TcParams {
     int num_seqs;     // varlen: sequences
     int compact;      // varlen: use the compact schedule table
     int num_items;    // num_mblk * num_splits * units_bh
+    int head_group;   // varlen compact order: heads per group
     float *ws_o;      // split mode: partial O, fp32 [splits][units][n][D]
     float *ws_l;      // split mode: partial L, fp32 [splits][units][n]
     float scale;
@@ -223,23 +227,31 @@ __device__ __forceinline__ void item_ranges(const TcParams &p, Item &it) {
 struct Sched {
     const uint16_t *ranked;   // [num_seqs] sequence ids, longest first
     const uint16_t *reach;    // [num_mblk] #sequences with more than L blocks
+    int per_head;             // items per head: the sum of reach over the levels
 };
 
-// Varlen compact order: level L from the top, then the sequences that reach
-// L (longest first), then heads -- only items that hold work, so the snake
-// assignment spreads real work evenly instead of walking empty slots.
+// Varlen compact order: heads in groups of p.head_group (a group's K and V
+// sized to stay in L2 while its items run); within a group, level L from
+// the top, then the sequences that reach L (longest first), then the
+// group's heads -- only items that hold work, so the snake assignment
+// spreads real work evenly instead of walking empty slots.
 template <bool WIN>
 __device__ __forceinline__ bool decode_varlen_compact(const TcParams &p, const Sched &sc, int idx,
                                                       Item &it) {
+    const int grp = idx / (sc.per_head * p.head_group);
+    idx -= grp * sc.per_head * p.head_group;
+    const int h0 = grp * p.head_group;
+    if (h0 >= p.heads) return false;
+    const int hn = min(p.head_group, p.heads - h0);
     int L = p.num_mblk - 1;
     for (; L >= 0; --L) {
-        const int here = (int)sc.reach[L] * p.heads;
+        const int here = (int)sc.reach[L] * hn;
         if (idx < here) break;
         idx -= here;
     }
     if (L < 0) return false;
-    const int seq = sc.ranked[idx / p.heads];
-    it.h = idx % p.heads;
+    const int seq = sc.ranked[idx / hn];
+    it.h = h0 + idx % hn;
     it.bh = 0;
     it.g = 0;
     it.mb = L;
@@ -380,13 +392,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < p.num_seqs; ++t) reach += nblk[t] > L;
             sched_reach[L] = (uint16_t)reach;
         }
+        if (threadIdx.x == 0) {
+            int total = 0;
+            for (int t = 0; t < p.num_seqs; ++t) total += nblk[t];
+            *reinterpret_cast<int *>(sched_reach + kMaxSchedLevels) = total;
+        }
         // generic-proxy use of the ring is over before TMA (async proxy) writes it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    const Sched sched{sched_ranked, sched_reach};
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const Sched sched{sched_ranked, sched_reach,
+                      p.compact ? *reinterpret_cast<const int *>(sched_reach + kMaxSchedLevels) : 0};
     const uint32_t tmem = *tmem_slot;
 
     const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
@@ -968,6 +986,13 @@ fa_status launch(const FaProblem &pr, int splits) {
     p.num_splits = splits;
     p.num_seqs = pr.num_seqs;
     p.compact = pr.varlen && pr.num_seqs <= kMaxSchedSeqs && p.num_mblk <= kMaxSchedLevels;
+    // Heads per group in the compact order: as many as keep the group's K
+    // and V within kL2GroupBytes.
+    {
+        const double kv_per_head = (double)pr.total * D * 2 * 2;
+        long long hg = kv_per_head > 0 ? (long long)(kL2GroupBytes / kv_per_head) : pr.heads;
+        p.head_group = (int)(hg < 1 ? 1 : (hg > pr.heads ? pr.heads : hg));
+    }
     const int64_t items = (int64_t)p.num_mblk * splits * pr.units_bh;
     if (items > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
     p.num_items = (int)items;
