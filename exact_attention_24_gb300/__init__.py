@@ -31,7 +31,7 @@ __all__ = [
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
     "attention_varlen", "EXPORTED_SYMBOLS", "fa_bwd", "fa_bwd_workspace_size",
-    "fa_bwd_varlen", "fa_bwd_varlen_workspace_size", "attention_bwd",
+    "fa_bwd_varlen", "fa_bwd_varlen_workspace_size", "fa_bwd_window", "attention_bwd",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, \
@@ -41,7 +41,7 @@ FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
                     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc",
-                    "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_varlen",
+                    "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_window", "fa_bwd_varlen",
                     "fa_bwd_varlen_workspace_size", "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
                     "fa_get_options", "fa_watchdog_selftest")
@@ -105,6 +105,9 @@ def load_library():
     lib.fa_bwd.restype = i32
     lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32]
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32,
+                                  i32, i32, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_window.restype = i32
     lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                   f32, i32, i32, vp, ctypes.c_size_t, vp]
     lib.fa_bwd_varlen.restype = i32
@@ -209,6 +212,14 @@ def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, D, scale, causal, dtype, work
 
 def fa_bwd_workspace_size(B, H, N) -> int:
     return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N)))
+
+
+def fa_bwd_window(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, D, scale, window_left, window_right,
+                  dtype, workspace, workspace_bytes, stream=None) -> int:
+    return load_library().fa_bwd_window(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
+        int(B), int(H), int(N), int(D), float(scale), int(window_left), int(window_right),
+        int(dtype), _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd_varlen(Q, K, V, O, dO, L, dQ, dK, dV, cu_seqlens, num_seqs, total_tokens, max_seqlen,

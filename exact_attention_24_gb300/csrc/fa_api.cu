@@ -174,7 +174,9 @@ fa_status fa_fwd_window(const void *Q, const void *K, const void *V, void *O, fl
                         int H, int N, int D, float scale, int window_left, int window_right,
                         fa_dtype dtype, fa_stream_t stream) {
     if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
-    return fwd_dense(Q, K, V, O, L, B, H, N, D, scale, 0, window_left, window_right, dtype, stream);
+    // (-1, 0) is the causal mask: the causal kernels skip the tiles above the diagonal
+    const int causal = window_left < 0 && window_right == 0;
+    return fwd_dense(Q, K, V, O, L, B, H, N, D, scale, causal, window_left, window_right, dtype, stream);
 }
 
 fa_status fa_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *L,
@@ -361,6 +363,46 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     p.causal = causal;
     p.wl = -1;
     p.wr = causal ? 0 : -1;
+    p.dtype = dtype;
+    p.stream = static_cast<cudaStream_t>(stream);
+    return run_bwd(p);
+}
+
+fa_status fa_bwd_window(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                        float scale, int window_left, int window_right, fa_dtype dtype,
+                        void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    const int64_t units = (int64_t)B * H;
+    if (units > INT32_MAX || (int64_t)N > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    const int64_t rows = units * N;
+    // (-1, 0) is the causal mask, (-1, -1) none: both run the plain kernels
+    const int causal = window_left < 0 && window_right == 0;
+    fa_status st = check_bwd(Q, K, V, O, dO, L, dQ, dK, dV, rows, D, scale, causal, dtype, workspace,
+                             workspace_bytes);
+    if (st != FA_OK || rows == 0) return st;
+    if (workspace_bytes < fa_bwd_workspace_size(B, H, N)) return FA_ERR_INVALID_ARG;
+    FaBwdProblem p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.dout = dO;
+    p.lse = L;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.delta = static_cast<float *>(workspace);
+    p.heads = H;
+    p.units_bh = (int)units;
+    p.n = N;
+    p.total = N;
+    p.D = D;
+    p.scale = scale;
+    p.causal = causal;
+    p.wl = window_left;
+    p.wr = window_right;
     p.dtype = dtype;
     p.stream = static_cast<cudaStream_t>(stream);
     return run_bwd(p);

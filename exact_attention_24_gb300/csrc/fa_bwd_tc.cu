@@ -48,6 +48,7 @@ struct BwdTcParams {
     int n, nblk;          // n: N, or the longest sequence of a packed batch
     float scale, scale_log2;
     int causal;
+    int wl, wr;           // band: key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     uint32_t *err;
     uint64_t wait_limit_ns;
 };
@@ -112,6 +113,20 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *tm, u
         else
             tma_load_3d(dst + hf * atom, tm, bar, hf * 64, row, q.unit);
     }
+}
+
+// Query rows a dK/dV item walks: [i_first, i_first + 64 * halves) covers
+// every row that sees some key of the block [j0, j0 + 128) (an even number
+// of 64-row halves).  Causal / full attention, or a band (WIN).
+template <bool WIN>
+__device__ __forceinline__ void dk_rows(const BwdTcParams &p, int j0, int n, int &i_first, int &halves) {
+    int lo = p.causal ? j0 : 0, hi = n;
+    if (WIN) {
+        lo = p.wr >= 0 ? max(0, j0 - p.wr) : 0;
+        hi = p.wl >= 0 ? min(n, j0 + kT + p.wl) : n;
+    }
+    i_first = lo;
+    halves = 2 * ((hi - lo + kT - 1) / kT);
 }
 
 // ------------------------------------------------------------ dK, dV --
@@ -199,7 +214,7 @@ __device__ __forceinline__ void issue_acc_half(uint32_t d_tmem, uint32_t a_tmem,
                (kk > 0 || accumulate) ? 1u : 0u);
 }
 
-template <int D, typename Tout>
+template <int D, typename Tout, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -262,8 +277,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             Seq sq;
             int j0;
             while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
-                const int i_first = p.causal ? j0 : 0;
-                const int halves = 2 * ((sq.len - i_first + kT - 1) / kT);
+                int i_first, halves;
+                dk_rows<WIN>(p, j0, sq.len, i_first, halves);
                 if (it > 0 && !mbar_wait(b.kv_free, (it - 1) & 1, wc, 0x40)) break;
                 mbar_arrive_expect_tx(b.fix_full, 2 * C::kTileBytes);
                 load_rows<D>(base, &tm_k, b.fix_full, j0, sq, p.varlen, kTcAtomBytes);
@@ -299,8 +314,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         Seq sq;
         int j0;
         while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
-            const int i_first = p.causal ? j0 : 0;
-            const int halves = 2 * ((sq.len - i_first + kT - 1) / kT);
+            int i_first, halves;
+            dk_rows<WIN>(p, j0, sq.len, i_first, halves);
             if (!warp_wait(b.fix_full, it & 1, wc, 0x50)) break;
             // S^T_x, dP^T_x of the item's first two halves (buffer x = half & 1)
             for (int u = 0; u < 2 && u < halves; ++u) {
@@ -367,8 +382,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int j0;
         while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
             const int n = sq.len;
-            const int i_first = p.causal ? j0 : 0;
-            const int halves = 2 * ((n - i_first + kT - 1) / kT);
+            int i_first, halves;
+            dk_rows<WIN>(p, j0, n, i_first, halves);
             const float *L = p.lse + sq.stat0;
             const float *Dl = p.delta + sq.stat0;
             // threads 0..63 stage the row statistics of query r of each half,
@@ -395,9 +410,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t t_st = t_s + x * 2 * 64, t_dpt = t_st + 64;
                 if (!warp_wait(b.s_full + 8 * x, (gu >> 1) & 1, wc, 0x60)) { ok = false; break; }
                 tc_fence_after();
-                // causal: query q sees key r iff q >= r; only the first tile holds
-                // queries below some key of the block
-                const bool diag = p.causal && u < 2;
+                // queries qi of this half that key r sees: qmin <= qi <= qmax.
+                // Causal: q >= r, which only the first tile can break; band:
+                // key - wr <= q <= key + wl, checked where a half crosses an edge.
+                int qmin, qmax;
+                bool diag;
+                if (WIN) {
+                    const int qb = i_first + 64 * u, key = j0 + r;
+                    qmin = p.wr >= 0 ? key - p.wr - qb : 0;
+                    qmax = p.wl >= 0 ? key + p.wl - qb : 63;
+                    diag = __any_sync(0xffffffffu, qmin > 0 || qmax < 63);
+                } else {
+                    diag = p.causal && u < 2;
+                    qmin = r - x * 64;
+                    qmax = 63;
+                }
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     float sv[32], dpv[32];
@@ -417,11 +444,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float2 p0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
                         float2 p1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
                         if (diag) {
-                            const int q = x * 64 + qi;
-                            if (q < r) p0.x = 0.f;
-                            if (q + 1 < r) p0.y = 0.f;
-                            if (q + 2 < r) p1.x = 0.f;
-                            if (q + 3 < r) p1.y = 0.f;
+                            if (qi < qmin || qi > qmax) p0.x = 0.f;
+                            if (qi + 1 < qmin || qi + 1 > qmax) p0.y = 0.f;
+                            if (qi + 2 < qmin || qi + 2 > qmax) p1.x = 0.f;
+                            if (qi + 3 < qmin || qi + 3 > qmax) p1.y = 0.f;
                         }
                         const float2 g0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dpv[e], dpv[e + 1]), make_float2(-d4.x, -d4.y)));
                         const float2 g1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dpv[e + 2], dpv[e + 3]), make_float2(-d4.z, -d4.w)));
@@ -515,12 +541,23 @@ __device__ __forceinline__ bool next_dq_item(const BwdTcParams &p, int &k, int c
     return false;
 }
 
-__device__ __forceinline__ int dq_tiles(const BwdTcParams &p, int ib, int len) {
+// Key tiles a dQ item walks: [t_lo, t_lo + tiles) covers every key that
+// some row of the block [128 ib, 128 ib + 128) sees.
+template <bool WIN>
+__device__ __forceinline__ void dq_tiles(const BwdTcParams &p, int ib, int len, int &t_lo, int &tiles) {
     const int key_tiles = (len + kT - 1) / kT;
-    return p.causal ? min(ib + 1, key_tiles) : key_tiles;
+    t_lo = 0;
+    tiles = p.causal ? min(ib + 1, key_tiles) : key_tiles;
+    if (WIN) {
+        const int i0 = ib * kT, il = min(len, i0 + kT) - 1;
+        const int lo = p.wl >= 0 ? max(0, i0 - p.wl) : 0;
+        const int hi = p.wr >= 0 ? min(len - 1, il + p.wr) : len - 1;
+        t_lo = lo / kT;
+        tiles = hi / kT + 1 - t_lo;
+    }
 }
 
-template <int D, typename Tout>
+template <int D, typename Tout, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -577,7 +614,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool ok = true;
             Seq sq;
             while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
-                const int tiles = dq_tiles(p, ib, sq.len);
+                int t_lo, tiles;
+                dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
                 if (it > 0 && !mbar_wait(qd_free, (it - 1) & 1, wc, 0x43)) break;
                 mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
                 load_rows<D>(base, &tm_q, fix_full, ib * kT, sq, p.varlen, kTcAtomBytes);
@@ -592,7 +630,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
                         load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
-                                     j * kT, sq, p.varlen, kTcAtomBytes);
+                                     (t_lo + j) * kT, sq, p.varlen, kTcAtomBytes);
                     }
                 }
             }
@@ -613,7 +651,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         Seq sq;
         while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
-            const int tiles = dq_tiles(p, ib, sq.len);
+            int t_lo, tiles;
+            dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
             // K_j is ring load lb + 2j, V_j load lb + 2j + 1; tile t uses S buffer (gt + t) & 1
             if (!warp_wait(fix_full, it & 1, wc, 0x54) || !ring_wait(kv_full, lb, C::kSlots, wc, 0x55) ||
                 !ring_wait(kv_full, lb + 1, C::kSlots, wc, 0x55))
@@ -683,19 +722,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         Seq sq;
         while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
             const int n = sq.len;
-            const int tiles = dq_tiles(p, ib, n);
+            int t_lo, tiles;
+            dq_tiles<WIN>(p, ib, n, t_lo, tiles);
             const int row = ib * kT + r;
             const float lrow = row < n ? p.lse[sq.stat0 + row] * kLog2e : INFINITY;
             const float drow = row < n ? p.delta[sq.stat0 + row] : 0.f;
-            // keys past the causal diagonal or past the end are masked
-            const int lim = p.causal ? min(row + 1, n) : n;
+            // keys outside [lim_lo, lim): past the causal diagonal, outside the
+            // band or past the end
+            int lim = p.causal ? min(row + 1, n) : n, lim_lo = 0;
+            if (WIN) {
+                lim = p.wr >= 0 ? min(row + p.wr + 1, n) : n;
+                lim_lo = p.wl >= 0 ? row - p.wl : 0;
+            }
             for (int t = 0; t < tiles; ++t) {
                 const uint32_t g = gt + t;
                 const uint32_t t_s = t_s0 + (g & 1) * kT;
                 if (!warp_wait(s_full, g & 1, wc, 0x70)) { ok = false; break; }
                 tc_fence_after();
-                const int key0 = t * kT;
-                const bool need_mask = key0 + kT > lim;
+                const int key0 = (t_lo + t) * kT;
+                const bool need_mask = key0 + kT > lim || (WIN && key0 < lim_lo);
 #pragma unroll
                 for (int cc = 0; cc < kT / 32; ++cc) {
                     float sv[32], dpv[32];
@@ -711,8 +756,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                         if (need_mask) {
                             const int key = key0 + cc * 32 + x;
-                            if (key >= lim) pp.x = 0.f;
-                            if (key + 1 >= lim) pp.y = 0.f;
+                            if (key >= lim || (WIN && key < lim_lo)) pp.x = 0.f;
+                            if (key + 1 >= lim || (WIN && key + 1 < lim_lo)) pp.y = 0.f;
                         }
                         const float2 gg = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
                         dk[x / 2] = pack_bf16x2(gg.x, gg.y);
@@ -760,7 +805,7 @@ fa_status prepare(K kernel, int smem) {
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
-template <int D, typename Tout>
+template <int D, typename Tout, bool WIN>
 fa_status launch(const FaBwdProblem &p) {
     // dense: dims {D, N, B*H}, a box is {64, rows, 1}; packed: dims
     // {D, H, total}, a box is {64, 1, rows}
@@ -791,25 +836,27 @@ fa_status launch(const FaBwdProblem &p) {
     k.scale = p.scale;
     k.scale_log2 = p.scale * kLog2e;
     k.causal = p.causal;
+    k.wl = p.wl;
+    k.wr = p.wr;
     k.err = p.err;
     k.wait_limit_ns = p.wait_limit_ns;
     const long long grid = (long long)k.nblk * p.units_bh;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
     static bool ready = false;  // per instantiation
     if (!ready) {
-        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout>, DkCfg<D>::kSmemBytes);
-        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout>, DqCfg<D>::kSmemBytes);
+        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes);
+        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes);
         if (st != FA_OK) return st;
         ready = true;
     }
     int grid_dk = p.grid_ctas > 0 ? p.grid_ctas : num_sms();   // persistent: one CTA per SM
     if (grid_dk <= 0) return FA_ERR_CUDA;
     if (grid_dk > grid) grid_dk = (int)grid;
-    bwd_dkdv_tc_kernel<D, Tout><<<grid_dk, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv, tdo64,
+    bwd_dkdv_tc_kernel<D, Tout, WIN><<<grid_dk, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv, tdo64,
                                                                                          k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    bwd_dq_tc_kernel<D, Tout><<<grid_dk, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    bwd_dq_tc_kernel<D, Tout, WIN><<<grid_dk, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
     e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
@@ -819,9 +866,14 @@ fa_status launch(const FaBwdProblem &p) {
 
 fa_status fa_launch_bwd_tc(const FaBwdProblem &p) {
     if (p.dtype == FA_F32) return FA_ERR_UNSUPPORTED;
-    if (p.wl >= 0 || (p.wr >= 0 && !(p.causal && p.wr == 0))) return FA_ERR_UNSUPPORTED;
     if ((int64_t)p.units_bh * p.n == 0) return FA_OK;
     const bool f32 = p.dtype == FA_BF16_OUT_F32;
-    if (p.D == 64) return f32 ? fa::launch<64, float>(p) : fa::launch<64, __nv_bfloat16>(p);
-    return f32 ? fa::launch<128, float>(p) : fa::launch<128, __nv_bfloat16>(p);
+    // the band instantiation serves windows other than causal (-1, 0) and full (-1, -1)
+    const bool win = p.wl >= 0 || p.wr > 0;
+    if (p.D == 64) {
+        if (win) return f32 ? fa::launch<64, float, true>(p) : fa::launch<64, __nv_bfloat16, true>(p);
+        return f32 ? fa::launch<64, float, false>(p) : fa::launch<64, __nv_bfloat16, false>(p);
+    }
+    if (win) return f32 ? fa::launch<128, float, true>(p) : fa::launch<128, __nv_bfloat16, true>(p);
+    return f32 ? fa::launch<128, float, false>(p) : fa::launch<128, __nv_bfloat16, false>(p);
 }

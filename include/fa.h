@@ -254,6 +254,20 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N);
 
 /*
+ * fa_bwd_window -- gradients of the band forward pass (fa_fwd_window): the
+ * operation of fa_bwd with key j visible to query i iff
+ * i - window_left <= j <= i + window_right (-1: that side unbounded).
+ * O and L must come from fa_fwd_window with the same window.  Arguments,
+ * layouts, workspace and errors as fa_bwd; window bounds >= -1
+ * (FA_ERR_INVALID_ARG otherwise).
+ */
+FA_API fa_status fa_bwd_window(const void *Q, const void *K, const void *V, const void *O,
+                               const void *dO, const float *L, void *dQ, void *dK, void *dV, int B,
+                               int H, int N, int D, float scale, int window_left, int window_right,
+                               fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                               fa_stream_t stream);
+
+/*
  * fa_bwd_varlen -- gradients of the packed-batch forward pass
  * (fa_fwd_varlen): the same operation as fa_bwd for every sequence and
  * head, with fa_fwd_varlen's layout.

@@ -240,3 +240,15 @@ def test_bwd_varlen_argument_checks(lib):
                             0) == fa.FA_OK
     if not torch.cuda.is_available():
         assert call() == fa.FA_ERR_CUDA
+
+
+def test_bwd_window_argument_checks(lib):
+    q, k, v, o, do, l, dq, dk, dv, ws = _bwd_ptrs()
+    nws = fa.fa_bwd_workspace_size(1, 1, 16)
+    bad = fa.FA_ERR_INVALID_ARG
+    args = (q, k, v, o, do, l, dq, dk, dv, 1, 1, 16, 64, 0.1)
+    assert fa.fa_bwd_window(*args, -2, 0, fa.FA_BF16, ws, nws, 0) == bad
+    assert fa.fa_bwd_window(*args, 3, -7, fa.FA_BF16, ws, nws, 0) == bad
+    assert fa.fa_bwd_window(*args, 3, 3, fa.FA_BF16, 0, nws, 0) == bad
+    if not torch.cuda.is_available():
+        assert fa.fa_bwd_window(*args, 3, 3, fa.FA_BF16, ws, nws, 0) == fa.FA_ERR_CUDA

@@ -219,3 +219,73 @@ def test_bwd_varlen_full_size_sampled():
         ref = attention_bwd_sampled(q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], w.scale, True, idx, idx)
         mine = [to_f64(got[0][a + idx, h]), to_f64(got[1][a + idx, h]), to_f64(got[2][a + idx, h])]
         assert_grads(mine, ref, fa.FA_BF16, f"varlen full s={s} h={h}")
+
+
+# ------------------------------------------------------------ local band --
+def run_bwd_window(q, k, v, o, do, lse, wl, wr, code, scale):
+    B, H, N, D = q.shape
+    odt = torch.bfloat16 if code == fa.FA_BF16 else torch.float32
+    grads = [torch.full((B, H, N, D), float("nan"), dtype=odt, device=q.device) for _ in range(3)]
+    nbytes = fa.fa_bwd_workspace_size(B, H, N)
+    ws = torch.full((max(nbytes, 16) // 4,), float("nan"), dtype=torch.float32, device=q.device)
+    st = fa.fa_bwd_window(q, k, v, o, do, lse, *grads, B, H, N, D, scale, wl, wr, code, ws, nbytes,
+                          None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    assert fa.fa_check_device_error(None) == fa.FA_OK
+    return grads
+
+
+def _window_inputs(B, H, N, D, window, seed):
+    w = Workload("wbwd", B, H, N, D, "bf16", False, seed)
+    q, k, v = make_inputs(w)
+    do = make_inputs(Workload("wdO", B, H, N, D, "bf16", False, seed + 50_000))[0]
+    o, lse = attention_ref(q, k, v, w.scale, False, window=window)
+    return w, q, k, v, do, torch.from_numpy(o).to(q.dtype), torch.from_numpy(lse).float()
+
+
+BWD_WINDOWS = [(1, 2, 1000, 64, 64, 64), (1, 1, 777, 128, 100, 30), (2, 1, 600, 128, 0, 0),
+               (1, 1, 2048, 128, 300, -1), (1, 2, 1500, 64, 5, 200), (1, 1, 513, 64, 127, 129),
+               (1, 1, 1024, 128, 256, 0), (1, 1, 300, 128, 1000, 1000)]
+
+
+@pytest.mark.parametrize("case", BWD_WINDOWS, ids=lambda c: "x".join(map(str, c)))
+def test_bwd_window_matches_oracle(kernel, case):
+    B, H, N, D, wl, wr = case
+    w, q, k, v, do, o, lse = _window_inputs(B, H, N, D, (wl, wr), seed=N + wl + 7)
+    ref = attention_bwd_ref(q, k, v, do, w.scale, False, window=(wl, wr))[:3]
+    dev = [x.to(DEV) for x in (q, k, v, o, do, lse)]
+    for code in BF16_CODES:
+        got = run_bwd_window(*dev, wl, wr, code, w.scale)
+        assert_grads([to_f64(x) for x in got], ref, code, f"{kernel} band {case} dt={code}")
+
+
+def test_bwd_window_special_cases_are_the_plain_paths(kernel):
+    """(-1, 0) is the causal backward and (-1, -1) the full one, bit for bit."""
+    for causal, window in ((True, (-1, 0)), (False, (-1, -1))):
+        w, q, k, v, do, o, lse = _bwd_inputs(1, 2, 900, 128, "bf16", causal, seed=17)
+        dev = [x.to(DEV) for x in (q, k, v, o, do, lse)]
+        a = run_bwd(*dev, causal, fa.FA_BF16, w.scale)
+        b = run_bwd_window(*dev, window[0], window[1], fa.FA_BF16, w.scale)
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+def test_bwd_window_sliding_full_size_sampled():
+    """A causal 4096-key sliding window over 32K tokens (the sliding-window
+    forward workload's shape, one head shown), sampled rows and keys."""
+    B, H, N, D, wl, wr = 1, 2, 32768, 128, 4096, 0
+    w = Workload("wbig", B, H, N, D, "bf16", False, 3)
+    q, k, v = make_inputs(w)
+    do = make_inputs(Workload("wbigdO", B, H, N, D, "bf16", False, 50_003))[0]
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    O = torch.empty_like(qd)
+    L = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    assert fa.fa_fwd_window(qd, kd, vd, O, L, B, H, N, D, w.scale, wl, wr, fa.FA_BF16, None) == fa.FA_OK
+    got = run_bwd_window(qd, kd, vd, O, dod, L, wl, wr, fa.FA_BF16, w.scale)
+    rng = np.random.default_rng(9)
+    idx = np.unique(np.concatenate([[0, 4095, 4096, N - 1], rng.integers(0, N, 12)]))
+    for h in range(H):
+        ref = attention_bwd_sampled(q[0, h], k[0, h], v[0, h], do[0, h], w.scale, False, idx, idx,
+                                    window=(wl, wr))
+        mine = [to_f64(got[0][0, h, idx]), to_f64(got[1][0, h, idx]), to_f64(got[2][0, h, idx])]
+        assert_grads(mine, ref, fa.FA_BF16, f"sliding full size h={h}")
