@@ -383,8 +383,6 @@ def bench_bwd(args, w, rank, world, local):
     from exact_attention_24_gb300.build import build
     from exact_attention_24_gb300.workloads import make_inputs
 
-    if w.varlen or w.window:
-        raise SystemExit("--bwd covers dense causal or full attention")
     build()
     fa.load_library()
     torch.cuda.set_device(local)
@@ -399,19 +397,39 @@ def bench_bwd(args, w, rank, world, local):
     l_b = q.numel() // w.D * 4
     per_copy = 5 * tensor_b + l_b + 3 * tensor_b
     copies = max(2, math.ceil(2 * L2_BYTES / per_copy) + 1)
-    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.N)
+    ws_bytes = (fa.fa_bwd_varlen_workspace_size(w.total, w.H) if w.varlen
+                else fa.fa_bwd_workspace_size(w.B, w.H, w.N))
     with torch.cuda.stream(stream):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32).to(dev) if w.varlen else None
         bufs = []
         for _ in range(copies):
             qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
-            O, L = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, stream=stream)
+            if w.varlen:
+                O, L = fa.attention_varlen(qd, kd, vd, cu, w.max_seqlen, causal=w.causal, scale=w.scale,
+                                           stream=stream)
+            elif w.window:
+                O = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+                L = torch.empty(shape[:-1], dtype=torch.float32, device=dev)
+                st = fa.fa_fwd_window(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, w.window[0],
+                                      w.window[1], code, stream)
+                if st != fa.FA_OK:
+                    raise fa.FaError(st, "fa_fwd_window")
+            else:
+                O, L = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, stream=stream)
             grads = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3)]
             bufs.append((qd, kd, vd, O, dod, L, *grads))
     torch.cuda.synchronize(dev)
 
     def call(b):
-        st = fa.fa_bwd(*b, w.B, w.H, w.N, w.D, w.scale, int(w.causal), code, ws, ws_bytes, stream)
+        if w.varlen:
+            st = fa.fa_bwd_varlen(*b, cu, len(w.lengths), w.total, w.max_seqlen, w.H, w.D, w.scale,
+                                  int(w.causal), code, ws, ws_bytes, stream)
+        elif w.window:
+            st = fa.fa_bwd_window(*b, w.B, w.H, w.N, w.D, w.scale, w.window[0], w.window[1], code, ws,
+                                  ws_bytes, stream)
+        else:
+            st = fa.fa_bwd(*b, w.B, w.H, w.N, w.D, w.scale, int(w.causal), code, ws, ws_bytes, stream)
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_bwd")
 
@@ -470,7 +488,19 @@ def bench_bwd(args, w, rank, world, local):
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, device=dev)
     barrier(world)
-    peak, _, peak_kind = load_peaks()
+    peak, hbm_peak, peak_kind = load_peaks()
+    # algorithmic bytes: Q, K, V, O, dO read, dQ, dK, dV written, L and delta
+    min_bytes = 8 * tensor_b + 2 * l_b
+    t_launch = ms_local / args.steps * 1e-3
+    if min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
+        roofline = {"bound": "hbm", "achieved": round(min_bytes / t_launch / 1e9, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(min_bytes / t_launch / 1e9 / hbm_peak, 4),
+                    "peak_source": f"hbm_gbs of {peak_kind}"}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
+    roofline["traffic"] = load_traffic("fa_bwd", w.name)
     return {
         "metric": METRIC_BWD,
         "value": round(value, 2),
@@ -485,15 +515,14 @@ def bench_bwd(args, w, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "pass": "backward", "B": w.B, "H": w.H, "N": w.N, "D": w.D,
-                   "causal": w.causal, "out_dtype": "bf16", "seed": w.seed,
+                   "causal": w.causal, "window": list(w.window) or None,
+                   "lengths": list(w.lengths) if w.varlen else None,
+                   "out_dtype": "bf16", "seed": w.seed,
                    "flops_per_step": flops,
                    "l2": f"inputs rotated over {copies} resident copies "
                          f"({copies * per_copy / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
-                     "traffic": load_traffic("fa_bwd", w.name)},
+        "roofline": roofline,
         "e2e": {"value": round(world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": 5 * tensor_b + l_b, "d2h_bytes_per_step": 3 * tensor_b,
                 "steps": e2e_steps},
@@ -514,10 +543,16 @@ def _bwd_oracle_sample(w, views, dos, it, count, seed):
     rows = np.sort(rng.choice(n, size=min(count, n), replace=False))
     keys = np.sort(rng.choice(n, size=min(count, n), replace=False))
     vis_r = w.visible_keys(rows, n)
-    vis_k = (n - keys) if w.causal else np.full(keys.shape, n)   # rows that see each key
+    # rows that see each key: i in [j - wr, j + wl], i >= j under the causal mask
+    wl, wr = w.window if w.window else (-1, -1)
+    lo = np.maximum(0, keys - wr) if wr >= 0 else np.zeros_like(keys)
+    if w.causal:
+        lo = np.maximum(lo, keys)
+    hi = np.minimum(n - 1, keys + wl) if wl >= 0 else np.full_like(keys, n - 1)
+    vis_k = np.maximum(hi - lo + 1, 0)
     fl = float(np.sum(3 * 2 * vis_r * w.D) + np.sum(4 * 2 * vis_k * w.D))
     t0 = time.perf_counter()
-    attention_bwd_sampled(q, k, v, dos[h], w.scale, w.causal, rows, keys)
+    attention_bwd_sampled(q, k, v, dos[h], w.scale, w.causal, rows, keys, window=tuple(w.window) or None)
     return fl, time.perf_counter() - t0, len(rows) + len(keys)
 
 
@@ -527,7 +562,7 @@ def _bwd_views(w):
     do = make_inputs(dataclasses.replace(w, seed=w.seed + 50_000))[0]
     qf, kf, vf, dof = (x.double().numpy() for x in (q, k, v, do))
     views = head_views(w, qf, kf, vf)
-    dos = [dof[b, h] for b in range(w.B) for h in range(w.H)]
+    dos = [x[0] for x in head_views(w, dof, dof, dof)]
     return views, dos
 
 
