@@ -79,6 +79,15 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
                  : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel in
+// the stream (if launched with programmatic stream serialization) start its
+// CTAs as this grid's CTAs retire; wait blocks until every prerequisite grid
+// has completed and its memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 struct WaitCtx {
     uint32_t *err;               // device error word
     volatile int *abort_flag;    // CTA-wide abort flag in shared memory

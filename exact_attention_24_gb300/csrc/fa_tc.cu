@@ -339,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // plain causal / full kernels keep the simpler fixed-start schedule.
     const int win_l = WIN ? p.wl : -1;
 
+    // The next launch may set up its CTAs while this grid's last ones run.
+    pdl_launch_dependents();
     if (warp == kProducerWarp && lane == 0) {
         mbar_init(bar_q_full, 1);
         mbar_init(bar_q_empty, 1);
@@ -364,6 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // Everything above touched only shared memory and TMEM: wait here for the
+    // previous kernel in the stream before any global memory access.
+    pdl_wait();
     // Varlen compact schedule: rank the sequences by block count and count
     // how many reach each block level.  The lengths are staged in the (not
     // yet used) K/V ring; TMA writes there only after the barrier below.
@@ -1021,8 +1026,21 @@ fa_status launch(const FaProblem &pr, int splits) {
     if (fattr.maxThreadsPerBlock < kThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(mq, mk, mv, p);
-    e = cudaGetLastError();
+    // Programmatic stream serialization: the CTAs of this launch may start
+    // (barrier and TMEM setup) while the previous kernel's last CTAs run;
+    // the kernel waits for it (griddepcontrol.wait) before reading memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = pr.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
