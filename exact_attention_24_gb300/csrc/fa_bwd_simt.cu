@@ -97,6 +97,10 @@ __device__ __forceinline__ bool visible(int i, int j, const BwdParams &p) {
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const T *o, const T *dout, float *delta,
                                                         int64_t rows, int D, int heads, int64_t total) {
+    // launched with programmatic stream serialization: the next kernel may
+    // start its setup now; this one waits for the previous before reading
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -350,15 +354,25 @@ fa_status fa_launch_bwd_delta(const FaBwdProblem &p) {
     if (rows == 0) return FA_OK;
     const int64_t grid = (rows + 7) / 8;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (p.dtype == FA_F32)
-        fa::bwd_delta_kernel<float><<<(int)grid, 256, 0, p.stream>>>(
-            static_cast<const float *>(p.o), static_cast<const float *>(p.dout), p.delta, rows, p.D, heads,
-            p.total);
+        e = cudaLaunchKernelEx(&cfg, fa::bwd_delta_kernel<float>, static_cast<const float *>(p.o),
+                               static_cast<const float *>(p.dout), p.delta, rows, p.D, heads, p.total);
     else
-        fa::bwd_delta_kernel<__nv_bfloat16><<<(int)grid, 256, 0, p.stream>>>(
-            static_cast<const __nv_bfloat16 *>(p.o), static_cast<const __nv_bfloat16 *>(p.dout),
-            p.delta, rows, p.D, heads, p.total);
-    const cudaError_t e = cudaGetLastError();
+        e = cudaLaunchKernelEx(&cfg, fa::bwd_delta_kernel<__nv_bfloat16>,
+                               static_cast<const __nv_bfloat16 *>(p.o),
+                               static_cast<const __nv_bfloat16 *>(p.dout), p.delta, rows, p.D, heads,
+                               p.total);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
