@@ -114,6 +114,52 @@ def load_traffic(kernel_tag: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+_NCU_BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+
+
+def record_traffic(csv_path: str, kernel_tag: str, workload: str, captured_with: str) -> dict:
+    """Sum dram__bytes_read.sum / dram__bytes_write.sum over every launch in
+    an `ncu --csv` capture (one forward launch, or the launches of one
+    backward step) and store them in profiles/traffic.json under the current
+    source digest, which `load_traffic` checks."""
+    import csv
+    from exact_attention_24_gb300.build import _digest
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rd = wr = 0.0
+    launches = set()
+    for row in csv.DictReader(lines):
+        name, unit = row["Metric Name"], row["Metric Unit"]
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        if unit not in _NCU_BYTE_UNITS:
+            raise ValueError(f"unexpected unit {unit!r} for {name}")
+        v = float(row["Metric Value"].replace(",", "")) * _NCU_BYTE_UNITS[unit]
+        launches.add(row["ID"])
+        if name == "dram__bytes_read.sum":
+            rd += v
+        else:
+            wr += v
+    if not launches:
+        raise ValueError(f"no DRAM byte metrics in {csv_path}")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    entry = {"source_digest": _digest(), "dram_bytes_per_launch": int(round(rd + wr)),
+             "dram_bytes_read": int(round(rd)), "dram_bytes_write": int(round(wr)),
+             "launches_summed": len(launches), "captured_with": captured_with,
+             "note": "1-pass metrics; ncu flushes the caches before each launch; O lines still "
+                     "dirty in L2 at kernel end are not counted as DRAM writes"}
+    rec[f"{kernel_tag}/{workload}"] = entry
+    with open(path, "w") as f:
+        json.dump(dict(sorted(rec.items())), f, indent=1)
+        f.write("\n")
+    return entry
+
+
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling in the background."""
@@ -778,6 +824,12 @@ def main(argv=None):
                     help="time the backward pass (fa_bwd) instead of the forward pass")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,D[,causal] instead of a named workload (bf16, seed 8)")
+    ap.add_argument("--record-traffic", default=None, metavar="NCU_CSV",
+                    help="store the DRAM bytes of an ncu --csv capture of this workload (one "
+                         "forward launch, or one backward step with --bwd) in "
+                         "profiles/traffic.json, then exit")
+    ap.add_argument("--captured-with", default="",
+                    help="the ncu command line of that capture, kept beside the numbers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -791,6 +843,11 @@ def main(argv=None):
         w = Workload(name, f[0], f[1], f[2], f[3], "bf16", causal, 8)
     else:
         w = WORKLOADS[args.workload]
+    if args.record_traffic:
+        e = record_traffic(args.record_traffic, "fa_bwd" if args.bwd else "fa_tc", w.name,
+                           args.captured_with)
+        print(json.dumps({f"{'fa_bwd' if args.bwd else 'fa_tc'}/{w.name}": e}), flush=True)
+        return 0
     rank, world, local = dist_env()
     if world != args.gpus:
         world = max(world, 1)
