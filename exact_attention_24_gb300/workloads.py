@@ -133,6 +133,24 @@ def make_inputs(w: Workload):
     return q.to(dt), k.to(dt), v.to(dt)
 
 
+def make_inputs_device(w: Workload, device, count: int = 3) -> list:
+    """``count`` tensors of the workload's shape (q, k, v, then any extra such
+    as dO), drawn on ``device`` from a generator there seeded with the
+    workload's seed, in the storage dtype.
+
+    For sizes whose CPU generation would take minutes (tensors past 2^31
+    elements).  The values differ from :func:`make_inputs` (another
+    generator); a test copies the slices the oracle needs to the host."""
+    g = torch.Generator(device).manual_seed(w.seed)
+    shape = (w.total, w.H, w.D) if w.varlen else (w.B, w.H, w.N, w.D)
+    dt = _TORCH_DTYPE[w.dtype]
+    out = [torch.randn(shape, generator=g, device=device, dtype=dt) for _ in range(count)]
+    if w.qk_mult != 1.0:
+        out[0].mul_(w.qk_mult)
+        out[1].mul_(w.qk_mult)
+    return out
+
+
 def varlen_lengths(num_seqs: int, lo: int, hi: int, len_seed: int) -> tuple:
     """Sequence lengths uniform in ``[lo, hi]`` (inclusive) from a seed."""
     rng = np.random.default_rng(len_seed)
