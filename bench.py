@@ -46,6 +46,10 @@ METRIC = "attention fwd TFLOP/s (bf16, causal & non-causal) and % of GB300 BF16 
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 FFMA (the C1 kernel): 152 SMs x 128 fp32 lanes x 2 flop per FFMA at the
+# 2.07 GHz maximum SM clock -- nominal unit counts and clock, not a measurement
+FFMA_PEAK_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
+FFMA_PEAK_SOURCE = "nominal FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"
 
 
 # ------------------------------------------------------------ distributed --
@@ -260,9 +264,12 @@ def bench_ours(args, w, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     q, k, v = make_inputs(dataclasses.replace(w, seed=rank_seed(w.seed, rank)))
-    code = fa.FA_BF16
+    f32 = w.dtype == "f32"                     # C1: fp32 in and out, the FFMA kernel
+    code = fa.FA_F32 if f32 else fa.FA_BF16
+    o_dtype = torch.float32 if f32 else torch.bfloat16
+    o_size = 4 if f32 else 2
     in_bytes = 3 * q.numel() * q.element_size()
-    out_b = q.numel() * 2 + q.numel() // w.D * 4
+    out_b = q.numel() * o_size + q.numel() // w.D * 4
     copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_b)) + 1)
     bufs = []
     l_shape = (w.H, w.total) if w.varlen else q.shape[:-1]
@@ -270,7 +277,7 @@ def bench_ours(args, w, rank, world, local):
         cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32).to(dev) if w.varlen else None
         for _ in range(copies):
             bufs.append((q.to(dev), k.to(dev), v.to(dev),
-                         torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+                         torch.empty(q.shape, dtype=o_dtype, device=dev),
                          torch.empty(l_shape, dtype=torch.float32, device=dev)))
     torch.cuda.synchronize(dev)
 
@@ -334,7 +341,7 @@ def bench_ours(args, w, rank, world, local):
     qh = q.pin_memory()
     kh = k.pin_memory()
     vh = v.pin_memory()
-    oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    oh = torch.empty(q.shape, dtype=o_dtype).pin_memory()
     lh = torch.empty(l_shape, dtype=torch.float32).pin_memory()
     qd, kd, vd, O, L = bufs[0]
 
@@ -362,9 +369,14 @@ def bench_ours(args, w, rank, world, local):
     e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     peak, hbm_peak, peak_kind = load_peaks()
-    min_bytes = w.min_bytes(2)
+    min_bytes = w.min_bytes(o_size)
     t_launch = ms_local / args.steps * 1e-3
-    if min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
+    if f32:
+        # FFMA kernel: plain fp32 ALU arithmetic against the nominal FFMA rate
+        roofline = {"bound": "alu", "achieved": round(achieved, 4), "peak": FFMA_PEAK_TFLOPS,
+                    "unit": "TFLOP/s", "frac": round(achieved / FFMA_PEAK_TFLOPS, 5),
+                    "peak_source": FFMA_PEAK_SOURCE}
+    elif min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
         roofline = {"bound": "hbm", "achieved": round(min_bytes / t_launch / 1e9, 1),
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(min_bytes / t_launch / 1e9 / hbm_peak, 4),
@@ -374,7 +386,7 @@ def bench_ours(args, w, rank, world, local):
                     "peak": peak, "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4),
                     "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
-    roofline["traffic"] = load_traffic("fa_tc", w.name)
+    roofline["traffic"] = load_traffic("fa_simt" if f32 else "fa_tc", w.name)
     rec = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -386,11 +398,11 @@ def bench_ours(args, w, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f32" if f32 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
                    "causal": w.causal, "window": list(w.window) or None,
-                   "out_dtype": "bf16", "seed": w.seed,
+                   "out_dtype": "f32" if f32 else "bf16", "seed": w.seed,
                    "lengths": list(w.lengths) if w.varlen else None,
                    "splits": args.splits,
                    "flops_per_step": flops,
@@ -404,7 +416,7 @@ def bench_ours(args, w, rank, world, local):
                "tile_model_bytes_64x64": io_model_bytes(w, 64, 64)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": in_bytes,
-                "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+                "d2h_bytes_per_step": oh.numel() * o_size + lh.numel() * 4,
                 "steps": e2e_steps},
         "gpu_launches": args.steps * (2 if args.splits not in (None, 1) and ws_bytes else 1),
         "clocks": sampler.summary(),
@@ -744,7 +756,7 @@ def host_info() -> dict:
     return {"cpu_model": model or os.uname().machine, "blas_threads": threads or "library default (all cores)"}
 
 
-def cpu_baseline(w, seconds: float, seed: int = 0):
+def cpu_baseline(w, seconds: float, seed: int = 0, one_core: bool = True):
     """Time the oracle as it stands on this host's cores, on a bounded sample
     of the workload's rows (float64; causal rows count only their keys)."""
     views = _f64_views(w)
@@ -760,10 +772,32 @@ def cpu_baseline(w, seconds: float, seed: int = 0):
         n_rows += len(picks)
         it += 1
     cores = len(os.sched_getaffinity(0))
-    return {"value": done_flops / t_total / 1e12, "unit": UNIT, "cores": cores,
-            "kind": "oracle", "host": host_info(),
-            "sample": f"{n_rows} query rows ({it} heads x up to {rows} random rows) of {w.name}, "
-                      f"float64 NumPy, {t_total:.1f} s"}
+    rec = {"value": done_flops / t_total / 1e12, "unit": UNIT, "cores": cores,
+           "kind": "oracle", "host": host_info(),
+           "sample": f"{n_rows} query rows ({it} heads x up to {rows} random rows) of {w.name}, "
+                     f"float64 NumPy, {t_total:.1f} s"}
+    if one_core and w.flops() < ONE_CORE_MAX_FLOPS:
+        rec["one_core"] = cpu_baseline_one_core(w, seconds)
+    return rec
+
+
+# workloads small enough that the oracle is also timed on one core (C1, C2)
+ONE_CORE_MAX_FLOPS = 1e10
+
+
+def cpu_baseline_one_core(w, seconds: float):
+    """The same oracle timing in a child process pinned to one core, with the
+    BLAS thread pools limited to one thread (set before NumPy loads)."""
+    from exact_attention_24_gb300.workloads import WORKLOADS
+    if WORKLOADS.get(w.name) is not w:
+        return None
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", w.name,
+                        "--cpu-one-core", "--cpu-seconds", str(seconds)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0 or not r.stdout.strip():
+        return {"error": (r.stderr.strip().splitlines() or ["no output"])[-1][:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def bench_reference(args, w, rank, world):
@@ -830,7 +864,15 @@ def main(argv=None):
                          "profiles/traffic.json, then exit")
     ap.add_argument("--captured-with", default="",
                     help="the ncu command line of that capture, kept beside the numbers")
+    ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.cpu_one_core:
+        # child of cpu_baseline_one_core: the oracle timing on the first allowed core
+        os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})
+        from exact_attention_24_gb300.workloads import WORKLOADS
+        rec = cpu_baseline(WORKLOADS[args.workload], args.cpu_seconds, one_core=False)
+        print(json.dumps(rec), flush=True)
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from exact_attention_24_gb300.workloads import WORKLOADS, Workload
