@@ -24,10 +24,9 @@
 namespace fa {
 namespace {
 
-constexpr int kBr = 64;      // query rows per CTA
 constexpr int kBc = 64;      // keys per K/V tile
-constexpr int kWarps = 8;    // rows per warp = kBr / kWarps
-constexpr int kRowsPerWarp = kBr / kWarps;
+constexpr int kWarps = 8;    // a CTA's query rows: kWarps x rows per warp (8, or 1
+                             // when the 64-row grid would leave SMs idle)
 
 struct SimtParams {
     const void *q, *k, *v;
@@ -51,16 +50,34 @@ __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) {
     *p = __float2bfloat16_rn(x);
 }
 
-// Copy `rows` rows of D elements (row stride `stride` elements) starting at
+// Copy ROWS rows of D elements (row stride `stride` elements) starting at
 // row `r0` of a head into shared memory as fp32 with row pitch `pitch`;
-// rows at or beyond `len` are zero-filled.
-template <int D, typename Tin>
+// rows at or beyond `len` are zero-filled.  Each thread issues its global
+// loads kBatch at a time into registers before storing them, so their
+// latencies overlap (a load cannot pass a shared-memory store that might
+// alias it).
+template <int D, int ROWS, typename Tin>
 __device__ __forceinline__ void load_tile(float *dst, int pitch, const Tin *src,
                                           int64_t stride, int r0, int len) {
-    for (int x = threadIdx.x; x < kBr * D; x += blockDim.x) {
-        const int r = x / D, c = x % D;
-        const int row = r0 + r;
-        dst[r * pitch + c] = row < len ? ld_f32(src + (int64_t)row * stride + c) : 0.f;
+    constexpr int kThreads = kWarps * 32;
+    constexpr int kElems = ROWS * D;
+    constexpr int kPer = (kElems + kThreads - 1) / kThreads;  // elements per thread
+    constexpr int kBatch = kPer < 8 ? kPer : 8;
+#pragma unroll
+    for (int i0 = 0; i0 < kPer; i0 += kBatch) {
+        float buf[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int x = threadIdx.x + (i0 + i) * kThreads;
+            const int row = r0 + x / D;
+            buf[i] = (i0 + i < kPer && x < kElems && row < len)
+                         ? ld_f32(src + (int64_t)row * stride + x % D) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int x = threadIdx.x + (i0 + i) * kThreads;
+            if (i0 + i < kPer && x < kElems) dst[(x / D) * pitch + x % D] = buf[i];
+        }
     }
 }
 
@@ -75,9 +92,10 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-template <int D, typename Tin, typename Tout>
-__global__ void __launch_bounds__(kWarps * 32)
+template <int D, int RPW, typename Tin, typename Tout>
+__global__ void __launch_bounds__(kWarps * 32, 2)
     fa_simt_kernel(SimtParams p) {
+    constexpr int kBr = RPW * kWarps;    // query rows per CTA
     extern __shared__ float smem[];
     float *sQ = smem;                    // [kBr][D]
     float *sK = sQ + kBr * D;            // [kBc][D + 1]  (padded: no bank conflicts)
@@ -110,12 +128,12 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int DC = D / 32;  // output columns per lane
 
-    load_tile<D>(sQ, D, Q, stride, q0, len);
+    load_tile<D, kBr>(sQ, D, Q, stride, q0, len);
 
-    float acc[kRowsPerWarp][DC];
-    float m[kRowsPerWarp], l[kRowsPerWarp];
+    float acc[RPW][DC];
+    float m[RPW], l[RPW];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
+    for (int r = 0; r < RPW; ++r) {
         m[r] = -INFINITY;
         l[r] = 0.f;
 #pragma unroll
@@ -127,12 +145,12 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int kv_lo = p.wl >= 0 ? max(0, q0 - p.wl) / kBc * kBc : 0;
     for (int kv0 = kv_lo; kv0 < kv_end; kv0 += kBc) {
         __syncthreads();  // previous tile fully consumed (and sQ written)
-        load_tile<D>(sK, D + 1, K, stride, kv0, len);
-        load_tile<D>(sV, D, V, stride, kv0, len);
+        load_tile<D, kBc>(sK, D + 1, K, stride, kv0, len);
+        load_tile<D, kBc>(sV, D, V, stride, kv0, len);
         __syncthreads();
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
-            const int row = warp * kRowsPerWarp + r;
+        for (int r = 0; r < RPW; ++r) {
+            const int row = warp * RPW + r;
             const int qi = q0 + row;
             if (qi >= len) continue;  // warp-uniform
             const float *qrow = sQ + row * D;
@@ -179,8 +197,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 
     Tout *O = static_cast<Tout *>(p.o) + base;
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-        const int qi = q0 + warp * kRowsPerWarp + r;
+    for (int r = 0; r < RPW; ++r) {
+        const int qi = q0 + warp * RPW + r;
         if (qi >= len) continue;
         const bool live = l[r] > 0.f;
         const float inv = live ? 1.f / l[r] : 0.f;
@@ -191,8 +209,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
-template <int D, typename Tin, typename Tout>
+template <int D, int RPW, typename Tin, typename Tout>
 fa_status launch(const FaProblem &pr) {
+    constexpr int kBr = RPW * kWarps;
     SimtParams p;
     p.q = pr.q;
     p.k = pr.k;
@@ -211,7 +230,7 @@ fa_status launch(const FaProblem &pr) {
     p.wr = pr.wr;
     p.err = pr.err;
     const size_t smem = sizeof(float) * (size_t)(kBr * D + kBc * (D + 1) + kBc * D);
-    auto kern = fa_simt_kernel<D, Tin, Tout>;
+    auto kern = fa_simt_kernel<D, RPW, Tin, Tout>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fa_cuda_fail(e);
     const int tiles = (pr.n + kBr - 1) / kBr;
@@ -221,21 +240,43 @@ fa_status launch(const FaProblem &pr) {
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 
-template <int D>
-fa_status launch_d(const FaProblem &pr) {
+template <int D, int RPW>
+fa_status launch_dt(const FaProblem &pr) {
     switch (pr.dtype) {
-        case FA_F32: return launch<D, float, float>(pr);
-        case FA_BF16: return launch<D, __nv_bfloat16, __nv_bfloat16>(pr);
-        case FA_BF16_OUT_F32: return launch<D, __nv_bfloat16, float>(pr);
+        case FA_F32: return launch<D, RPW, float, float>(pr);
+        case FA_BF16: return launch<D, RPW, __nv_bfloat16, __nv_bfloat16>(pr);
+        case FA_BF16_OUT_F32: return launch<D, RPW, __nv_bfloat16, float>(pr);
         default: return FA_ERR_INVALID_ARG;
     }
+}
+
+// Streaming multiprocessors of the current device (0 if the query fails,
+// which keeps the 64-row grid).
+int sm_count() {
+    static int sms = -1;
+    if (sms < 0) {
+        int dev = 0, n = 0;
+        sms = (cudaGetDevice(&dev) == cudaSuccess &&
+               cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) ? n : 0;
+    }
+    return sms;
+}
+
+// 64-row CTAs (8 rows a warp) unless that grid leaves SMs idle; then 8-row
+// CTAs (one row a warp), 8x the CTAs.  Each row's arithmetic is the same
+// either way, so the results do not depend on the choice.
+template <int D>
+fa_status launch_d(const FaProblem &pr) {
+    const int64_t blocks64 = (int64_t)pr.units_bh * ((pr.n + 8 * kWarps - 1) / (8 * kWarps));
+    const bool small = blocks64 < sm_count() && (pr.n + kWarps - 1) / kWarps <= 65535;
+    return small ? launch_dt<D, 1>(pr) : launch_dt<D, 8>(pr);
 }
 
 }  // namespace
 }  // namespace fa
 
 fa_status fa_launch_simt(const FaProblem &pr) {
-    if ((pr.n + fa::kBr - 1) / fa::kBr > 65535) return FA_ERR_UNSUPPORTED;
+    if ((pr.n + 8 * fa::kWarps - 1) / (8 * fa::kWarps) > 65535) return FA_ERR_UNSUPPORTED;
     if (pr.D == 64) return fa::launch_d<64>(pr);
     if (pr.D == 128) return fa::launch_d<128>(pr);
     return FA_ERR_UNSUPPORTED;

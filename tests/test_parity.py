@@ -253,6 +253,26 @@ def test_grid_size_does_not_change_results():
         assert torch.equal(O, res[0][0]) and torch.equal(L, res[0][1])
 
 
+@pytest.mark.parametrize("code", [fa.FA_F32, fa.FA_BF16])
+def test_ffma_row_grouping_does_not_change_results(code):
+    """The FFMA kernel gives small grids one row per warp (8-row CTAs) and
+    larger ones 8 rows per warp (64-row CTAs); each row's arithmetic is the
+    same, so one head computed alone (4 blocks of 64 rows: under-filled) and
+    as head 0 of a 64-head batch (256 blocks) agree bitwise."""
+    dt = "f32" if code == fa.FA_F32 else "bf16"
+    w, q, k, v = _dense_case(1, 64, 256, 64, dt, True, seed=13)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    assert fa.fa_set_options(fa.FA_KERNEL_SIMT, 0, 0) == fa.FA_OK
+    try:
+        O_all, L_all = run_dense(qd, kd, vd, True, code, w.scale)
+        O_one, L_one = run_dense(*(x[:, :1].contiguous() for x in (qd, kd, vd)), True, code, w.scale)
+    finally:
+        fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+    assert torch.equal(O_one[:, 0], O_all[:, 0]) and torch.equal(L_one[:, 0], L_all[:, 0])
+    ref_o, ref_l = attention_ref(q[0, 0], k[0, 0], v[0, 0], w.scale, True)
+    assert_close(to_f64(O_one[0, 0]), to_f64(L_one[0, 0]), ref_o, ref_l, code, "FFMA one row a warp")
+
+
 def test_invalid_cu_seqlens_reported_on_device(kernel):
     """A decreasing cu_seqlens is caught on the device: the sequence is
     skipped and fa_check_device_error reports FA_ERR_INVALID_ARG."""
