@@ -103,9 +103,9 @@ def load_peaks():
 
 
 def load_traffic(kernel_tag: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel
-    source has not changed since it was taken (else None)."""
-    from exact_attention_24_gb300.build import _digest
+    """DRAM bytes per launch from a committed ncu summary, if the sources of
+    that kernel family have not changed since it was taken (else None)."""
+    from exact_attention_24_gb300.build import kernel_digest
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -113,7 +113,7 @@ def load_traffic(kernel_tag: str, workload: str):
     except (OSError, ValueError):
         return None
     e = rec.get(f"{kernel_tag}/{workload}")
-    if not e or e.get("source_digest") != _digest():
+    if not e or e.get("source_digest") != kernel_digest(kernel_tag):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -125,9 +125,9 @@ def record_traffic(csv_path: str, kernel_tag: str, workload: str, captured_with:
     """Sum dram__bytes_read.sum / dram__bytes_write.sum over every launch in
     an `ncu --csv` capture (one forward launch, or the launches of one
     backward step) and store them in profiles/traffic.json under the current
-    source digest, which `load_traffic` checks."""
+    digest of that kernel family's sources, which `load_traffic` checks."""
     import csv
-    from exact_attention_24_gb300.build import _digest
+    from exact_attention_24_gb300.build import kernel_digest
     with open(csv_path) as f:
         lines = [ln for ln in f if ln.startswith('"')]
     rd = wr = 0.0
@@ -152,7 +152,7 @@ def record_traffic(csv_path: str, kernel_tag: str, workload: str, captured_with:
             rec = json.load(f)
     except (OSError, ValueError):
         rec = {}
-    entry = {"source_digest": _digest(), "dram_bytes_per_launch": int(round(rd + wr)),
+    entry = {"source_digest": kernel_digest(kernel_tag), "dram_bytes_per_launch": int(round(rd + wr)),
              "dram_bytes_read": int(round(rd)), "dram_bytes_write": int(round(wr)),
              "launches_summed": len(launches), "captured_with": captured_with,
              "note": "1-pass metrics; ncu flushes the caches before each launch; O lines still "

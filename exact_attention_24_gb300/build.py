@@ -43,15 +43,36 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _digest() -> str:
+# Sources that decide what one kernel family does, besides the shared
+# headers, the ABI header and the API file (which picks kernels and launch
+# parameters): a measurement of a family stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "fa_tc": ("fa_tc.cu",),
+    "fa_simt": ("fa_simt.cu",),
+    "fa_bwd": ("fa_bwd_tc.cu", "fa_bwd_simt.cu"),
+}
+_SHARED = ("device_common.cuh", "tc_common.cuh", "fa_internal.h", "fa_api.cu")
+
+
+def _hash(paths) -> str:
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(CSRC, "*")) +
-                       glob.glob(os.path.join(INCLUDE, "*.h"))):
+    for path in sorted(paths):
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
             h.update(f.read())
     h.update(" ".join(NVCC_FLAGS).encode())
     return h.hexdigest()[:16]
+
+
+def _digest() -> str:
+    """Digest of every source of the library (the build stamp)."""
+    return _hash(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h")))
+
+
+def kernel_digest(kernel: str) -> str:
+    """Digest of the sources one kernel family depends on (see KERNEL_SOURCES)."""
+    names = KERNEL_SOURCES[kernel] + _SHARED
+    return _hash([os.path.join(CSRC, n) for n in names] + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

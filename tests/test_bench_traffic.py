@@ -75,3 +75,23 @@ def test_capture_without_dram_metrics_is_rejected(bench_in_tmp):
     csv.write_text(HEADER + _row(0, "k", "gpu__time_duration.sum", "ns", "8"))
     with pytest.raises(ValueError):
         bench.record_traffic(str(csv), "fa_tc", "W4", "")
+
+
+def test_kernel_digest_follows_only_its_own_sources(tmp_path, monkeypatch):
+    """Editing one kernel family's source leaves the other families'
+    measurements valid; editing a shared header invalidates them all."""
+    import shutil
+    from exact_attention_24_gb300 import build
+    csrc = tmp_path / "csrc"
+    shutil.copytree(build.CSRC, csrc)
+    monkeypatch.setattr(build, "CSRC", str(csrc))
+    before = {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES}
+    with open(csrc / "fa_simt.cu", "a") as f:
+        f.write("\n// edit\n")
+    after = {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES}
+    assert after["fa_simt"] != before["fa_simt"]
+    assert after["fa_tc"] == before["fa_tc"] and after["fa_bwd"] == before["fa_bwd"]
+    with open(csrc / "device_common.cuh", "a") as f:
+        f.write("\n// edit\n")
+    shared = {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES}
+    assert all(shared[k] != after[k] for k in build.KERNEL_SOURCES)
