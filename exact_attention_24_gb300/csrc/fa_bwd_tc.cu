@@ -842,13 +842,12 @@ fa_status launch(const FaBwdProblem &p) {
     k.wait_limit_ns = p.wait_limit_ns;
     const long long grid = (long long)k.nblk * p.units_bh;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
-    static bool ready = false;  // per instantiation
-    if (!ready) {
-        fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes);
-        if (st == FA_OK) st = prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes);
-        if (st != FA_OK) return st;
-        ready = true;
-    }
+    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
+    const fa_status su = fa_once_per_device(ready, []() -> fa_status {
+        const fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes);
+        return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes) : st;
+    });
+    if (su != FA_OK) return su;
     int grid_dk = p.grid_ctas > 0 ? p.grid_ctas : num_sms();   // persistent: one CTA per SM
     if (grid_dk <= 0) return FA_ERR_CUDA;
     if (grid_dk > grid) grid_dk = (int)grid;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/fa.h"
 
 // Device error word layout: bits 31..24 = fa_status code, bits 15..0 = the
@@ -67,6 +69,23 @@ struct FaBwdProblem {
 // fa_last_cuda_error) and clear the runtime's sticky-free last error.
 // Returns FA_ERR_CUDA so launchers can `return fa_cuda_fail(e);`.
 fa_status fa_cuda_fail(cudaError_t e);
+
+// Run `setup` (kernel attributes: dynamic shared memory and the like) once
+// per device and kernel instantiation; `done` is that instantiation's mask
+// of devices already set up.  Launches after the first then make no runtime
+// calls besides the launch itself, so they can also be captured in a CUDA
+// graph.  Returns the first failure of `setup`, which is retried next time.
+template <typename F>
+inline fa_status fa_once_per_device(std::atomic<uint64_t> &done, F &&setup) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return FA_OK;
+    const fa_status st = setup();
+    if (st == FA_OK && bit) done.fetch_or(bit, std::memory_order_release);
+    return st;
+}
 
 fa_status fa_launch_simt(const FaProblem &p);
 // Backward pass: delta = rowsum(dO * O), then the FFMA or tensor-core

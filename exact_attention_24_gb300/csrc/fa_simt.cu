@@ -231,12 +231,16 @@ fa_status launch(const FaProblem &pr) {
     p.err = pr.err;
     const size_t smem = sizeof(float) * (size_t)(kBr * D + kBc * (D + 1) + kBc * D);
     auto kern = fa_simt_kernel<D, RPW, Tin, Tout>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fa_cuda_fail(e);
+    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
+    const fa_status su = fa_once_per_device(ready, [&]() -> fa_status {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
+    });
+    if (su != FA_OK) return su;
     const int tiles = (pr.n + kBr - 1) / kBr;
     dim3 grid(pr.units_bh, tiles);
     kern<<<grid, kWarps * 32, smem, pr.stream>>>(p);
-    e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
 

@@ -1020,12 +1020,16 @@ fa_status launch(const FaProblem &pr, int splits) {
     if (grid <= 0) return FA_ERR_CUDA;  // device query failed (recorded)
     if (grid > p.num_items) grid = p.num_items;
     auto kern = fa_tc_kernel<D, OUT, WIN>;
-    cudaFuncAttributes fattr;
-    cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
-    if (e != cudaSuccess) return fa_cuda_fail(e);
-    if (fattr.maxThreadsPerBlock < kThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return fa_cuda_fail(e);
+    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
+    const fa_status su = fa_once_per_device(ready, [&]() -> fa_status {
+        cudaFuncAttributes fattr;
+        cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
+        if (e != cudaSuccess) return fa_cuda_fail(e);
+        if (fattr.maxThreadsPerBlock < kThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
+    });
+    if (su != FA_OK) return su;
     // Programmatic stream serialization: the CTAs of this launch may start
     // (barrier and TMEM setup) while the previous kernel's last CTAs run;
     // the kernel waits for it (griddepcontrol.wait) before reading memory.
@@ -1039,7 +1043,7 @@ fa_status launch(const FaProblem &pr, int splits) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
