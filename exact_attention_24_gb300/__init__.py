@@ -28,6 +28,7 @@ __all__ = [
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_TC", "FaError",
     "load_library", "library_path", "fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
     "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
+    "fa_fwd_host",
     "fa_check_device_error", "fa_status_string", "fa_last_cuda_error", "fa_set_options",
     "fa_get_options", "fa_watchdog_selftest", "attention",
     "attention_varlen", "EXPORTED_SYMBOLS", "fa_bwd", "fa_bwd_workspace_size",
@@ -40,7 +41,7 @@ FA_F32, FA_BF16, FA_BF16_OUT_F32 = 0, 1, 2
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_TC = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_window", "fa_fwd_varlen", "fa_fwd_splitkv",
-                    "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc",
+                    "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv_noalloc", "fa_fwd_host",
                     "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_window", "fa_bwd_varlen",
                     "fa_bwd_varlen_workspace_size", "fa_check_device_error",
                     "fa_status_string", "fa_last_cuda_error", "fa_set_options",
@@ -100,6 +101,9 @@ def load_library():
     lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
                                            i32, i32, i32, vp]
     lib.fa_fwd_splitkv_noalloc.restype = i32
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                i32, i32, i32, vp]
+    lib.fa_fwd_host.restype = i32
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32,
                            i32, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i32
@@ -182,6 +186,17 @@ def fa_fwd_splitkv(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, num_splits,
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), int(B), int(H), int(N), int(D),
         float(scale), int(causal), int(dtype), int(num_splits), _ptr(workspace),
         int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_host(Qh, Kh, Vh, Oh, Lh, Qd, Kd, Vd, Od, Ld, B, H, N, D, scale, causal, dtype,
+                chunks, stream=None) -> int:
+    """Forward pass on HOST tensors (pinned for overlap) through caller-owned
+    device staging buffers, copies overlapped with the kernels of
+    neighbouring runs of ``chunks`` (see include/fa.h)."""
+    return load_library().fa_fwd_host(
+        _ptr(Qh), _ptr(Kh), _ptr(Vh), _ptr(Oh), _ptr(Lh), _ptr(Qd), _ptr(Kd), _ptr(Vd), _ptr(Od),
+        _ptr(Ld), int(B), int(H), int(N), int(D), float(scale), int(causal), int(dtype),
+        int(chunks), _stream(stream))
 
 
 def fa_fwd_splitkv_noalloc(Q, K, V, O, L, B, H, N, D, scale, causal, dtype, num_splits,

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -50,6 +51,45 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
+}
+
+// fa_fwd_host's copy streams and run events, created on a device's first call
+// and kept for the process; g_pipe_mu also serialises the enqueueing.
+constexpr int kMaxHostChunks = 64;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t landed[kMaxHostChunks], computed[kMaxHostChunks];
+};
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mu;
+
+// The current device's pipe (g_pipe_mu held), or null after recording the failure.
+HostPipe *host_pipe() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+        return nullptr;
+    }
+    HostPipe &hp = g_pipes[dev];
+    if (hp.ready) return &hp;
+    const unsigned ev = cudaEventDisableTiming;
+    e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, ev);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.end, ev);
+    for (int i = 0; e == cudaSuccess && i < kMaxHostChunks; ++i) {
+        e = cudaEventCreateWithFlags(&hp.landed[i], ev);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.computed[i], ev);
+    }
+    if (e != cudaSuccess) {  // partial creations are kept and retried no further
+        fa_cuda_fail(e);
+        return nullptr;
+    }
+    hp.ready = true;
+    return &hp;
 }
 
 size_t in_bytes(int dtype) { return dtype == FA_F32 ? 4 : 2; }
@@ -168,6 +208,72 @@ static fa_status fwd_dense(const void *Q, const void *K, const void *V, void *O,
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
                  int N, int D, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
     return fwd_dense(Q, K, V, O, L, B, H, N, D, scale, causal, -1, causal ? 0 : -1, dtype, stream);
+}
+
+fa_status fa_fwd_host(const void *Qh, const void *Kh, const void *Vh, void *Oh, float *Lh, void *Qd,
+                      void *Kd, void *Vd, void *Od, float *Ld, int B, int H, int N, int D, float scale,
+                      int causal, fa_dtype dtype, int chunks, fa_stream_t stream) {
+    if (chunks < 1 || chunks > kMaxHostChunks || B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    const int64_t units = (int64_t)B * H;
+    fa_status st = check_common(Qd, Kd, Vd, Od, Ld, units, N, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    if (units == 0 || N == 0) return FA_OK;
+    if (!Qh || !Kh || !Vh || !Oh || !Lh) return FA_ERR_INVALID_ARG;
+    // runs of whole problems; boundaries on multiples of g keep each run's L
+    // slice (u0 * N floats in) 16-byte aligned
+    const int64_t g = N % 4 == 0 ? 1 : (N % 2 == 0 ? 2 : 4);
+    const int64_t blocks = (units + g - 1) / g;
+    const int runs = (int)(chunks < blocks ? chunks : blocks);
+    const size_t row_in = (size_t)N * D * in_bytes(dtype), row_out = (size_t)N * D * out_bytes(dtype);
+    const size_t row_l = (size_t)N * sizeof(float);
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *hp = host_pipe();
+    if (!hp) return FA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(hp->start, s);  // earlier work on `stream` first
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    for (int c = 0; c < runs && st == FA_OK; ++c) {
+        const int64_t u0 = blocks * c / runs * g, u1 = std::min(units, blocks * (c + 1) / runs * g);
+        const size_t n = (size_t)(u1 - u0);
+        auto dev = [&](void *base, size_t row) { return static_cast<char *>(base) + (size_t)u0 * row; };
+        auto host = [&](const void *base, size_t row) {
+            return static_cast<const char *>(base) + (size_t)u0 * row;
+        };
+        e = cudaMemcpyAsync(dev(Qd, row_in), host(Qh, row_in), n * row_in, cudaMemcpyHostToDevice, hp->in);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev(Kd, row_in), host(Kh, row_in), n * row_in, cudaMemcpyHostToDevice, hp->in);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev(Vd, row_in), host(Vh, row_in), n * row_in, cudaMemcpyHostToDevice, hp->in);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->landed[c], hp->in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->landed[c], 0);
+        if (e != cudaSuccess) {
+            st = fa_cuda_fail(e);
+            break;
+        }
+        st = fwd_dense(dev(Qd, row_in), dev(Kd, row_in), dev(Vd, row_in), dev(Od, row_out),
+                       reinterpret_cast<float *>(dev(Ld, row_l)), 1, (int)n, N, D, scale, causal, -1,
+                       causal ? 0 : -1, dtype, stream);
+        if (st != FA_OK) break;
+        e = cudaEventRecord(hp->computed[c], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->computed[c], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(Oh) + (size_t)u0 * row_out, dev(Od, row_out), n * row_out,
+                                cudaMemcpyDeviceToHost, hp->out);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<char *>(Lh) + (size_t)u0 * row_l, dev(Ld, row_l), n * row_l,
+                                cudaMemcpyDeviceToHost, hp->out);
+        if (e != cudaSuccess) st = fa_cuda_fail(e);
+    }
+    // `stream` completes after the last copy in either direction, also on a
+    // failure, so no copy outlives the caller's view of the buffers
+    cudaError_t e2 = cudaEventRecord(hp->end, hp->out);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, hp->end, 0);
+    if (e2 == cudaSuccess) e2 = cudaEventRecord(hp->start, hp->in);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, hp->start, 0);
+    if (e2 != cudaSuccess && st == FA_OK) st = fa_cuda_fail(e2);
+    return st;
 }
 
 fa_status fa_fwd_window(const void *Q, const void *K, const void *V, void *O, float *L, int B,

@@ -210,6 +210,47 @@ FA_API fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void
                                         int num_splits, fa_stream_t stream);
 
 /*
+ * fa_fwd_host -- fa_fwd for inputs and outputs in HOST memory, with the
+ * transfers overlapped with the computation.  The dense batch is cut into
+ * `chunks` runs of consecutive (batch, head) problems.  Each run's Q, K, V go
+ * host -> device on a copy stream, its forward pass runs on `stream` once
+ * they have landed, and its O, L go device -> host on a second copy stream,
+ * so both copy directions overlap the kernels of the neighbouring runs.  The
+ * pages have no counterpart: this changes where the data lives, not what is
+ * computed (the results are bitwise those of fa_fwd on the same data).
+ *
+ *   Qh, Kh, Vh : HOST [B, H, N, D] inputs.  Pinned memory (cudaHostAlloc or
+ *                cudaHostRegister) gives the overlap; pageable memory works
+ *                without it.
+ *   Oh, Lh     : HOST outputs, [B, H, N, D] and [B, H, N] fp32
+ *   Qd, Kd, Vd, Od, Ld : caller-owned DEVICE buffers of the full sizes (the
+ *                staging area; same layout, alignment and overlap rules as
+ *                fa_fwd's arguments).  Their contents on exit are the
+ *                inputs and outputs of the pass.
+ *   B, H, N, D, scale, causal, dtype : as fa_fwd
+ *   chunks     : 1..64 runs (fewer if B*H is smaller).  Run boundaries fall
+ *                on multiples of 4 / gcd(N, 4) problems, keeping every
+ *                run's L slice 16-byte aligned.
+ *   stream     : when the work on `stream` completes, Oh and Lh hold the
+ *                results; the call itself returns after enqueueing.  Host
+ *                buffers must stay valid until then.
+ *
+ * The two copy streams and the events that order the runs are created on a
+ * device's first call and kept until the process exits.  Calls on one device
+ * are enqueued under a lock and share them: concurrent calls are correct but
+ * their runs serialise on the copy streams.
+ *
+ * Errors: FA_ERR_INVALID_ARG for a null host pointer, chunks outside 1..64
+ * or any fa_fwd argument error, before anything is enqueued;
+ * FA_ERR_UNSUPPORTED as fa_fwd; FA_ERR_CUDA if a copy, event or launch fails
+ * (the stream still waits for every copy already enqueued).
+ */
+FA_API fa_status fa_fwd_host(const void *Qh, const void *Kh, const void *Vh, void *Oh,
+                             float *Lh, void *Qd, void *Kd, void *Vd, void *Od, float *Ld,
+                             int B, int H, int N, int D, float scale, int causal,
+                             fa_dtype dtype, int chunks, fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the dense forward pass.  Given dO (the gradient of
  * a loss with respect to O), the forward inputs Q, K, V and the forward
  * outputs O and L, compute

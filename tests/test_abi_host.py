@@ -252,3 +252,24 @@ def test_bwd_window_argument_checks(lib):
     assert fa.fa_bwd_window(*args, 3, 3, fa.FA_BF16, 0, nws, 0) == bad
     if not torch.cuda.is_available():
         assert fa.fa_bwd_window(*args, 3, 3, fa.FA_BF16, ws, nws, 0) == fa.FA_ERR_CUDA
+
+
+def test_host_forward_argument_checks(lib):
+    """fa_fwd_host rejects bad arguments before any copy is enqueued: chunk
+    counts outside 1..64, null host buffers and every fa_fwd check of the
+    device staging buffers."""
+    qd, kd, vd, od, ld = _ptrs()
+    qh, kh, vh, oh, lh = (A + (10 + i) * STEP for i in range(5))
+    bad = fa.FA_ERR_INVALID_ARG
+    dims = (2, 3, 100, 64, 0.1, 1, fa.FA_BF16)
+    for chunks in (0, -1, 65):
+        assert fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, *dims, chunks, 0) == bad
+    assert fa.fa_fwd_host(0, kh, vh, oh, lh, qd, kd, vd, od, ld, *dims, 4, 0) == bad
+    assert fa.fa_fwd_host(qh, kh, vh, oh, 0, qd, kd, vd, od, ld, *dims, 4, 0) == bad
+    assert fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, 0, ld, *dims, 4, 0) == bad
+    assert fa.fa_fwd_host(qh, kh, vh, oh, lh, qd + 8, kd, vd, od, ld, *dims, 4, 0) == bad
+    assert fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, qd + 64, ld, *dims, 4, 0) == bad
+    assert fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, 2, 3, 100, 96, 0.1, 1,
+                          fa.FA_BF16, 4, 0) == fa.FA_ERR_UNSUPPORTED
+    # empty batches are no-ops, host pointers unused
+    assert fa.fa_fwd_host(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 3, 100, 64, 0.1, 1, fa.FA_BF16, 4, 0) == fa.FA_OK
