@@ -519,7 +519,7 @@ struct DqCfg {
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(8 * (2 + 2 * kSlots + 5) + 16 <= kBarBytes, "barrier area");
+    static_assert(8 * (2 + 2 * kSlots + 7) + 16 <= kBarBytes, "barrier area");
     static_assert(3 * kT + D <= (int)kTmemCols, "TMEM columns");
 };
 
@@ -569,7 +569,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t bars = base + C::kBarOff;
     const uint32_t fix_full = bars, qd_free = bars + 8, kv_full = bars + 16, kv_empty = kv_full + 8 * C::kSlots;
-    const uint32_t s_full = kv_empty + 8 * C::kSlots, ds_full = s_full + 8, o_final = ds_full + 8;
+    // s_full[2]: S of tile g ready in TMEM buffer g & 1 (phase (g >> 1) & 1);
+    // dp_full: dP of tile g ready (phase g & 1).  Separate barriers let the dS
+    // step compute P from S while dP is still being computed.
+    const uint32_t s_full = kv_empty + 8 * C::kSlots, dp_full = s_full + 16, ds_full = dp_full + 8;
+    const uint32_t o_final = ds_full + 8;
     const uint32_t acc_free = o_final + 8, drain = acc_free + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
@@ -584,6 +588,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(kv_empty + 8 * i, 1);
         }
         mbar_init(s_full, 1);
+        mbar_init(s_full + 8, 1);
+        mbar_init(dp_full, 1);
         mbar_init(ds_full, 4);
         mbar_init(o_final, 1);
         mbar_init(acc_free, 4);
@@ -660,8 +666,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             if (elect_one()) {
                 issue_qk<D>(tmem + (gt & 1) * kT, d_q, d_ring_k + (lb % C::kSlots) * kTileDesc);   // S_0
+                mma_commit(s_full + 8 * (gt & 1));
                 issue_qk<D>(t_dp, d_do, d_ring_k + ((lb + 1) % C::kSlots) * kTileDesc);            // dP_0
-                mma_commit(s_full);
+                mma_commit(dp_full);
                 mma_commit(kv_empty + 8 * ((lb + 1) % C::kSlots));                                // V_0 read
                 if (tiles == 1) mma_commit(qd_free);                                            // Q, dO read
             }
@@ -669,8 +676,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (tiles > 1) {
                 if (!ring_wait(kv_full, lb + 2, C::kSlots, wc, 0x55)) break;
                 tc_fence_after();
-                if (elect_one())
+                if (elect_one()) {
                     issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + ((lb + 2) % C::kSlots) * kTileDesc);
+                    mma_commit(s_full + 8 * ((gt + 1) & 1));                                    // S_1
+                }
                 __syncwarp();
             }
             for (int t = 0; t < tiles; ++t) {
@@ -685,7 +694,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (elect_one()) {
                     if (t + 1 < tiles) {
                         issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
-                        mma_commit(s_full);
+                        mma_commit(dp_full);
                         mma_commit(kv_empty + 8 * (lvn % C::kSlots));
                         if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
                     }
@@ -696,7 +705,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (t + 2 < tiles) {
                     if (!ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) { ok = false; break; }
                     tc_fence_after();
-                    if (elect_one()) issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
+                    if (elect_one()) {
+                        issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
+                        mma_commit(s_full + 8 * (g & 1));
+                    }
                     __syncwarp();
                 }
             }
@@ -737,28 +749,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int t = 0; t < tiles; ++t) {
                 const uint32_t g = gt + t;
                 const uint32_t t_s = t_s0 + (g & 1) * kT;
-                if (!warp_wait(s_full, g & 1, wc, 0x70)) { ok = false; break; }
+                if (!warp_wait(s_full + 8 * (g & 1), (g >> 1) & 1, wc, 0x70)) { ok = false; break; }
                 tc_fence_after();
                 const int key0 = (t_lo + t) * kT;
                 const bool need_mask = key0 + kT > lim || (WIN && key0 < lim_lo);
+                // P = exp2(S c - L) for the whole row while dP may still be computed
+                float pv[kT];
+#pragma unroll
+                for (int cc = 0; cc < kT / 32; ++cc) tmem_ld32(t_s + cc * 32, pv + cc * 32);
+                tmem_wait_ld();
+                const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
+                const float2 nd2 = make_float2(-drow, -drow);
+#pragma unroll
+                for (int x = 0; x < kT; x += 2) {
+                    const float2 a = __ffma2_rn(make_float2(pv[x], pv[x + 1]), c2, nl2);
+                    float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                    if (need_mask) {
+                        const int key = key0 + x;
+                        if (key >= lim || (WIN && key < lim_lo)) pp.x = 0.f;
+                        if (key + 1 >= lim || (WIN && key + 1 < lim_lo)) pp.y = 0.f;
+                    }
+                    pv[x] = pp.x;
+                    pv[x + 1] = pp.y;
+                }
+                if (!warp_wait(dp_full, g & 1, wc, 0x72)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < kT / 32; ++cc) {
-                    float sv[32], dpv[32];
-                    tmem_ld32(t_s + cc * 32, sv);
+                    float dpv[32];
                     tmem_ld32(t_dp + cc * 32, dpv);
                     tmem_wait_ld();
                     uint32_t dk[16];
-                    const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
-                    const float2 nd2 = make_float2(-drow, -drow);
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
-                        const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), c2, nl2);
-                        float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-                        if (need_mask) {
-                            const int key = key0 + cc * 32 + x;
-                            if (key >= lim || (WIN && key < lim_lo)) pp.x = 0.f;
-                            if (key + 1 >= lim || (WIN && key + 1 < lim_lo)) pp.y = 0.f;
-                        }
+                        const float2 pp = make_float2(pv[cc * 32 + x], pv[cc * 32 + x + 1]);
                         const float2 gg = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
                         dk[x / 2] = pack_bf16x2(gg.x, gg.y);
                     }
