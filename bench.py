@@ -817,29 +817,35 @@ def bench_reference(args, w, rank, world):
     if rank != 0:
         return None
     views = _f64_views(w)
-    # size each step so that warm-up + steps stay within ~90 s
-    picks, _ = oracle_rows_sample(w, views[0], 16, 0)
-    t0 = time.perf_counter()
-    run_oracle_sample(w, views[0], picks)
-    per_row = max((time.perf_counter() - t0) / len(picks), 1e-6)
+    # each step: 64-row samples of successive heads (the size cpu_baseline
+    # uses) until the step's share of ~90 s is spent
+    rows = 64
     budget = 90.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, budget / per_row))
+
+    def step(seed):
+        t, fl, it = 0.0, 0.0, 0
+        while t < budget:
+            view = views[(seed + it) % len(views)]
+            p, f = oracle_rows_sample(w, view, rows, 10_000 * seed + it)
+            t0 = time.perf_counter()
+            run_oracle_sample(w, view, p)
+            t += time.perf_counter() - t0
+            fl += f
+            it += 1
+        return t, fl, it
+
     for i in range(args.warmup):
-        view = views[i % len(views)]
-        p, _ = oracle_rows_sample(w, view, rows, 10_000 + i)
-        run_oracle_sample(w, view, p)
-    t_total, fl_total = 0.0, 0.0
+        step(1_000 + i)
+    t_total, fl_total, n_samples = 0.0, 0.0, 0
     for i in range(args.steps):
-        view = views[i % len(views)]
-        p, fl = oracle_rows_sample(w, view, rows, i)
-        t0 = time.perf_counter()
-        run_oracle_sample(w, view, p)
-        t_total += time.perf_counter() - t0
+        t, fl, it = step(i)
+        t_total += t
         fl_total += fl
+        n_samples += it
     value = fl_total / t_total / 1e12
     cores = len(os.sched_getaffinity(0))
-    sample = (f"up to {rows} random query rows of one head per step, {args.steps} steps, "
-              f"of {w.name}; float64 NumPy oracle")
+    sample = (f"{n_samples} samples of up to {rows} random query rows of one head, over {args.steps} "
+              f"steps of ~{budget:.0f} s each, of {w.name}; float64 NumPy oracle")
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
