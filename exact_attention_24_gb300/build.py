@@ -56,11 +56,13 @@ _SHARED = ("device_common.cuh", "tc_common.cuh", "fa_internal.h", "fa_api.cu")
 
 def _hash(paths) -> str:
     h = hashlib.sha256()
-    for path in sorted(paths):
+    for path in sorted(paths, key=os.path.basename):
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
             h.update(f.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    # the flags without the checkout's location, so that a copy of the tree
+    # elsewhere (another machine) has the same digest
+    h.update(" ".join(f.replace(INCLUDE, "<include>") for f in NVCC_FLAGS).encode())
     return h.hexdigest()[:16]
 
 

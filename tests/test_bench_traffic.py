@@ -95,3 +95,20 @@ def test_kernel_digest_follows_only_its_own_sources(tmp_path, monkeypatch):
         f.write("\n// edit\n")
     shared = {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES}
     assert all(shared[k] != after[k] for k in build.KERNEL_SOURCES)
+
+
+def test_kernel_digest_does_not_depend_on_the_checkout_location(tmp_path, monkeypatch):
+    """A copy of the tree at another path (as on another machine) has the same
+    digests, so measurements recorded in one place stay valid in another."""
+    import shutil
+    from exact_attention_24_gb300 import build
+    here = {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES}
+    csrc, inc = tmp_path / "pkg" / "csrc", tmp_path / "include"
+    shutil.copytree(build.CSRC, csrc)
+    shutil.copytree(build.INCLUDE, inc)
+    monkeypatch.setattr(build, "CSRC", str(csrc))
+    monkeypatch.setattr(build, "INCLUDE", str(inc))
+    monkeypatch.setattr(build, "NVCC_FLAGS", [f.replace(build.ROOT + "/include", str(inc))
+                                              for f in build.NVCC_FLAGS])
+    assert any(str(inc) in f for f in build.NVCC_FLAGS)
+    assert {k: build.kernel_digest(k) for k in build.KERNEL_SOURCES} == here
