@@ -1,8 +1,9 @@
 """Build the in-tree shared library ``libfa_gb300.so`` for sm_103a.
 
 Each translation unit under ``csrc/`` is compiled by its own ``nvcc`` process
-(in parallel), then linked with the static CUDA runtime, so the library loads
-on machines without a GPU driver (the driver API entry point it needs,
+(in parallel), then linked against the CUDA toolkit's shared runtime (found
+through an rpath).  The runtime loads the GPU driver lazily, so the library
+loads on machines without one (the driver API entry point it needs,
 ``cuTensorMapEncodeTiled``, is looked up at run time through the runtime).
 
 Usage: ``python -m exact_attention_24_gb300.build [--force] [--verbose]``.
