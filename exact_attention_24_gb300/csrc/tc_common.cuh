@@ -4,6 +4,8 @@
 // host-side TMA map encoder.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -118,17 +120,24 @@ inline bool make_map(CUtensorMap *m, const void *ptr, int D, uint64_t d1, uint64
     return true;
 }
 
+// Streaming multiprocessors of the current device, cached per device; 0
+// (with the failure recorded) if the device cannot be queried.
 inline int num_sms() {
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            fa_cuda_fail(e);
-            sms = 0;
-        }
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+        return 0;
     }
+    int sms = cached[dev].load(std::memory_order_relaxed);
+    if (sms > 0) return sms;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        fa_cuda_fail(e);
+        return 0;
+    }
+    cached[dev].store(sms, std::memory_order_relaxed);
     return sms;
 }
 
