@@ -87,6 +87,27 @@ inline fa_status fa_once_per_device(std::atomic<uint64_t> &done, F &&setup) {
     return st;
 }
 
+// Streaming multiprocessors of the current device, cached per device; 0
+// (with the failure recorded) if the device cannot be queried.
+inline int fa_num_sms() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+        return 0;
+    }
+    int sms = cached[dev].load(std::memory_order_relaxed);
+    if (sms > 0) return sms;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        fa_cuda_fail(e);
+        return 0;
+    }
+    cached[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
 fa_status fa_launch_simt(const FaProblem &p);
 // Backward pass: delta = rowsum(dO * O), then the FFMA or tensor-core
 // gradient kernels (each launcher runs the delta kernel itself).

@@ -254,17 +254,6 @@ fa_status launch_dt(const FaProblem &pr) {
     }
 }
 
-// Streaming multiprocessors of the current device (0 if the query fails,
-// which keeps the 64-row grid).
-int sm_count() {
-    static int sms = -1;
-    if (sms < 0) {
-        int dev = 0, n = 0;
-        sms = (cudaGetDevice(&dev) == cudaSuccess &&
-               cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) ? n : 0;
-    }
-    return sms;
-}
 
 // 64-row CTAs (8 rows a warp) unless that grid leaves SMs idle; then 8-row
 // CTAs (one row a warp), 8x the CTAs.  Each row's arithmetic is the same
@@ -272,7 +261,7 @@ int sm_count() {
 template <int D>
 fa_status launch_d(const FaProblem &pr) {
     const int64_t blocks64 = (int64_t)pr.units_bh * ((pr.n + 8 * kWarps - 1) / (8 * kWarps));
-    const bool small = blocks64 < sm_count() && (pr.n + kWarps - 1) / kWarps <= 65535;
+    const bool small = blocks64 < fa_num_sms() && (pr.n + kWarps - 1) / kWarps <= 65535;
     return small ? launch_dt<D, 1>(pr) : launch_dt<D, 8>(pr);
 }
 

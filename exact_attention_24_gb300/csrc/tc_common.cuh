@@ -4,8 +4,6 @@
 // host-side TMA map encoder.
 #pragma once
 
-#include <atomic>
-
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -84,9 +82,10 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint6
 }
 
 // ------------------------------------------------------------ host side --
+// The driver's tensor-map encoder, looked up once (thread-safe static
+// initialisation); null, with the failure recorded, if the driver lacks it.
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
@@ -95,8 +94,9 @@ inline PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
             fa_cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
             return nullptr;
         }
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    if (!fn) fa_cuda_fail(cudaErrorSymbolNotFound);
     return fn;
 }
 
@@ -120,25 +120,6 @@ inline bool make_map(CUtensorMap *m, const void *ptr, int D, uint64_t d1, uint64
     return true;
 }
 
-// Streaming multiprocessors of the current device, cached per device; 0
-// (with the failure recorded) if the device cannot be queried.
-inline int num_sms() {
-    static std::atomic<int> cached[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
-        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
-        return 0;
-    }
-    int sms = cached[dev].load(std::memory_order_relaxed);
-    if (sms > 0) return sms;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) {
-        fa_cuda_fail(e);
-        return 0;
-    }
-    cached[dev].store(sms, std::memory_order_relaxed);
-    return sms;
-}
+inline int num_sms() { return fa_num_sms(); }
 
 }  // namespace fa
