@@ -820,7 +820,7 @@ def bench_reference(args, w, rank, world):
     # each step: 64-row samples of successive heads (the size cpu_baseline
     # uses) until the step's share of ~90 s is spent
     rows = 64
-    budget = 90.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
 
     def step(seed):
         t, fl, it = 0.0, 0.0, 0
@@ -885,6 +885,8 @@ def main(argv=None):
                     help="the ncu command line of that capture, kept beside the numbers")
     ap.add_argument("--e2e-runs", type=int, default=E2E_RUNS,
                     help="runs that fa_fwd_host cuts a dense batch into for the e2e measurement")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="seconds of oracle time that --impl reference spreads over its steps")
     ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.cpu_one_core:

@@ -95,3 +95,29 @@ def test_two_rank_split_key_exchange():
     for rank in range(2):
         eo, el = out[rank]
         assert eo < 1e-12 and el < 1e-12
+
+
+def _run_bench(rank, world, *args):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], env=env,
+                          capture_output=True, text=True, timeout=300)
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_prints_on_rank_zero_only():
+    """Under torchrun the reference arm (the float64 oracle on the host) runs
+    and prints on rank 0 alone; the other ranks exit 0 without output."""
+    import json
+    args = ("--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3",
+            "--workload", "B1_H1_N256_D64_f32", "--ref-seconds", "1")
+    r1 = _run_bench(1, 2, *args)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = _run_bench(0, 2, *args)
+    assert r0.returncode == 0, r0.stderr[-500:]
+    rec = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert rec["impl"] == "reference" and rec["value"] > 0 and rec["steps"] == 2
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+    assert rec["cpu_baseline"]["value"] == rec["value"]
