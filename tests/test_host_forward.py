@@ -74,3 +74,19 @@ def test_host_forward_orders_after_earlier_stream_work():
     done.synchronize()
     O, L = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=w.scale)
     assert torch.equal(oh, O.cpu()) and torch.equal(lh, L.cpu())
+
+
+def test_host_forward_with_pageable_memory():
+    """Pageable (not pinned) host tensors give the same results; the copies
+    then do not overlap, but correctness does not depend on pinning."""
+    B, H, N, D = 2, 3, 300, 64
+    w = Workload("host3", B, H, N, D, "bf16", False, 44)
+    q, k, v = make_inputs(w)
+    oh = torch.full(q.shape, float("nan"), dtype=q.dtype)
+    lh = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32)
+    stage = [torch.empty_like(q, device=DEV) for _ in range(4)] + [torch.empty(q.shape[:-1], device=DEV)]
+    st = fa.fa_fwd_host(q, k, v, oh, lh, *stage, B, H, N, D, w.scale, 0, fa.FA_BF16, 3, None)
+    assert st == fa.FA_OK, fa.fa_status_string(st) + " / " + fa.fa_last_cuda_error()
+    torch.cuda.synchronize()
+    O, L = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=False, scale=w.scale)
+    assert torch.equal(oh, O.cpu()) and torch.equal(lh, L.cpu())
