@@ -30,8 +30,8 @@
 // Online softmax details (all per row, in registers of the row's thread):
 //   scores stay unscaled; exponentials are exp2(S*c - m*c), c = scale*log2 e
 //   the running max m is only moved (and l, O rescaled) when the new max
-//   exceeds it by more than 8 in log2 units; otherwise the stale m is kept,
-//   which is exact (l and O share the same reference) and bounds P by 2^8.
+//   exceeds it by more than 16 in log2 units; otherwise the stale m is kept,
+//   which is exact (l and O share the same reference) and bounds P by 2^16.
 //
 // Every mbarrier wait is bounded (device_common.cuh): a stuck pipeline is
 // reported as FA_ERR_DEVICE_TIMEOUT and the CTA drains its copies and MMAs,
@@ -53,7 +53,7 @@ constexpr int kThreads = 320;       // 10 warps
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 16.0f;  // log2 units
 // Epilogue destinations.
 constexpr int kOutBf16 = 0;   // O bf16, L
 constexpr int kOutF32 = 1;    // O fp32, L
