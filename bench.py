@@ -20,6 +20,15 @@ buffers, host->device copies of Q, K, V and device->host copies of O, L
 inside the timed region.  ``--impl reference`` times the float64 CPU oracle
 (the only reference implementation there is) on a bounded sample of rows.
 
+The default run (this workload, one GPU) adds three objects to the line:
+``per_config`` times the other benchmark workloads (C1, C2, C4, C5) the same
+way, each for at least ``--config-seconds`` of device time so that the clock
+sampler (NVML, read every 2 ms; nvidia-smi where NVML does not load) sees
+its timed region; ``sustained`` repeats this workload for at least
+``--sustained-seconds`` and sets its rate against the sustained bf16 peak,
+with the median SM clock and the cycles per step; ``e2e.host_link_gbs`` is
+the raw pinned host <-> device copy rate that bounds the end-to-end leg.
+
 Under ``torchrun`` (N > 1) every rank runs its own copy of the workload on
 its own GPU (weak scaling, independent problems, no collective on the data
 path); the time is the max over ranks.
@@ -51,6 +60,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FFMA_PEAK_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 FFMA_PEAK_SOURCE = "nominal FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"
 E2E_RUNS = 4          # fa_fwd_host runs in the end-to-end measurement of a dense batch
+HEADLINE = "B2_H16_N4096_D128_bf16_causal"
 
 
 # ------------------------------------------------------------ distributed --
@@ -242,6 +252,99 @@ class ClockSampler:
                 "in_timed_region": in_region}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read from NVML (libnvidia-ml, through
+    ctypes) every few milliseconds in a background thread, so that even a
+    timed region of a few milliseconds holds samples.  Reads only; sets
+    nothing.  ``ok`` is False where NVML cannot be loaded (then the
+    nvidia-smi sampler above is used)."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_id: str, period_s: float = 0.002):
+        import ctypes
+        self.period = period_s
+        self.samples = []          # (time, sm_mhz, reason mask)
+        self.marks = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if gpu_id.isdigit():
+                r = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(gpu_id)), ctypes.byref(h))
+            else:
+                r = lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(h))
+            if r != 0:
+                return
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.lib, self.h, self.ctypes = lib, h, ctypes
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        ct = self.ctypes
+        mhz, mask = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if (self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0 and
+                    self.reason_fn(self.h, ct.byref(mask)) == 0):
+                self.samples.append((time.time(), float(mhz.value), int(mask.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 2:
+                time.sleep(0.001)
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        self._stop.set()
+        if self.ok:
+            self.thread.join(timeout=2)
+
+    def summary(self, region=None):
+        """Median SM clock and the reasons seen between two marks (``region``
+        = their indices, default the first and last); all samples if none
+        fell inside."""
+        if not self.samples:
+            return None
+        rows = []
+        if len(self.marks) >= 2:
+            a, b = region or (0, len(self.marks) - 1)
+            t0, t1 = self.marks[a], self.marks[b]
+            rows = [x for x in self.samples if t0 <= x[0] <= t1]
+        in_region = bool(rows)
+        rows = rows or self.samples
+        reasons = set()
+        for _, _, m in rows:
+            for bit, name in self.REASONS.items():
+                if m & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(rows), "in_timed_region": in_region,
+                "source": "nvml"}
+
+
+def make_sampler(gpu_id: str):
+    """The NVML sampler where NVML loads, else nvidia-smi."""
+    s = NvmlSampler(gpu_id)
+    return s if s.ok else ClockSampler(gpu_id)
+
+
 def smi_gpu_id(local: int) -> str:
     """nvidia-smi --id for CUDA device `local` (honours CUDA_VISIBLE_DEVICES)."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -253,50 +356,58 @@ def smi_gpu_id(local: int) -> str:
 
 
 # ------------------------------------------------------------- our arm --
-def bench_ours(args, w, rank, world, local):
-    import torch
-    import exact_attention_24_gb300 as fa
-    from exact_attention_24_gb300.build import build
-    from exact_attention_24_gb300.workloads import make_inputs
+class FwdRunner:
+    """A workload's inputs resident on the device, rotated over enough copies
+    that the bytes touched between two uses of one copy exceed twice the L2
+    (every launch starts with a cold L2), and the library call that runs one
+    step (one forward pass over the whole workload) on ``stream``."""
 
-    build()
-    fa.load_library()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.Stream(device=dev)
-    q, k, v = make_inputs(dataclasses.replace(w, seed=rank_seed(w.seed, rank)))
-    f32 = w.dtype == "f32"                     # C1: fp32 in and out, the FFMA kernel
-    code = fa.FA_F32 if f32 else fa.FA_BF16
-    o_dtype = torch.float32 if f32 else torch.bfloat16
-    o_size = 4 if f32 else 2
-    in_bytes = 3 * q.numel() * q.element_size()
-    out_b = q.numel() * o_size + q.numel() // w.D * 4
-    copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_b)) + 1)
-    bufs = []
-    l_shape = (w.H, w.total) if w.varlen else q.shape[:-1]
-    with torch.cuda.stream(stream):
-        cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32).to(dev) if w.varlen else None
-        for _ in range(copies):
-            bufs.append((q.to(dev), k.to(dev), v.to(dev),
-                         torch.empty(q.shape, dtype=o_dtype, device=dev),
-                         torch.empty(l_shape, dtype=torch.float32, device=dev)))
-    torch.cuda.synchronize(dev)
+    def __init__(self, fa, w, dev, stream, seed, splits=None):
+        import torch
+        from exact_attention_24_gb300.workloads import make_inputs
+        self.fa, self.w, self.dev, self.stream, self.splits = fa, w, dev, stream, splits
+        q, k, v = make_inputs(dataclasses.replace(w, seed=seed))
+        self.host = (q, k, v)
+        self.f32 = w.dtype == "f32"                 # C1: fp32 in and out, the FFMA kernel
+        self.code = fa.FA_F32 if self.f32 else fa.FA_BF16
+        self.o_dtype = torch.float32 if self.f32 else torch.bfloat16
+        self.o_size = 4 if self.f32 else 2
+        self.in_bytes = 3 * q.numel() * q.element_size()
+        self.out_bytes = q.numel() * self.o_size + q.numel() // w.D * 4
+        self.copies = max(2, math.ceil(2 * L2_BYTES / (self.in_bytes + self.out_bytes)) + 1)
+        self.l_shape = (w.H, w.total) if w.varlen else q.shape[:-1]
+        self.bufs = []
+        with torch.cuda.stream(stream):
+            self.cu = torch.as_tensor(w.cu_seqlens, dtype=torch.int32).to(dev) if w.varlen else None
+            for _ in range(self.copies):
+                self.bufs.append((q.to(dev), k.to(dev), v.to(dev),
+                                  torch.empty(q.shape, dtype=self.o_dtype, device=dev),
+                                  torch.empty(self.l_shape, dtype=torch.float32, device=dev)))
+        self.ws, self.ws_bytes = None, 0
+        if splits is not None:
+            self.ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.D, splits)
+            self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
 
-    ws = None
-    ws_bytes = 0
-    if args.splits is not None:
-        ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.D, args.splits)
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    @property
+    def launches_per_step(self) -> int:
+        return 2 if self.splits not in (None, 1) and self.ws_bytes else 1
 
-    def call(qd, kd, vd, O, L):
-        if args.splits is not None:
+    @property
+    def l2_note(self) -> str:
+        return (f"inputs rotated over {self.copies} resident copies "
+                f"({self.copies * (self.in_bytes + self.out_bytes) / 1e6:.0f} MB > 129 MB L2)")
+
+    def call(self, qd, kd, vd, O, L):
+        fa, w, stream, code = self.fa, self.w, self.stream, self.code
+        if self.splits is not None:
             st = fa.fa_fwd_splitkv(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
-                                   code, args.splits, ws, ws_bytes, stream)
+                                   code, self.splits, self.ws, self.ws_bytes, stream)
         elif w.window:
             st = fa.fa_fwd_window(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, w.window[0],
                                   w.window[1], code, stream)
         elif w.varlen:
-            st = fa.fa_fwd_varlen(qd, kd, vd, O, L, cu, len(w.lengths), w.total, w.max_seqlen,
+            st = fa.fa_fwd_varlen(qd, kd, vd, O, L, self.cu, len(w.lengths), w.total, w.max_seqlen,
                                   w.H, w.D, w.scale, int(w.causal), code, stream)
         else:
             st = fa.fa_fwd(qd, kd, vd, O, L, w.B, w.H, w.N, w.D, w.scale, int(w.causal),
@@ -304,38 +415,84 @@ def bench_ours(args, w, rank, world, local):
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
 
-    def launch(i):
-        call(*bufs[i % copies])
+    def launch(self, i):
+        self.call(*self.bufs[i % self.copies])
+
+    def check(self, what):
+        st = self.fa.fa_check_device_error(self.stream)
+        if st != self.fa.FA_OK:
+            raise self.fa.FaError(st, what)
+
+    def timed(self, steps, sampler=None, world=1):
+        """Device time (ms) of `steps` launches between two CUDA events on
+        the launching stream, with a barrier and a synchronize on both sides;
+        the sampler's marks bracket the region."""
+        import torch
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        if sampler:
+            sampler.mark()
+        ev0.record(self.stream)
+        for i in range(steps):
+            self.launch(i)
+        ev1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        if sampler:
+            sampler.mark()
+        barrier(world)
+        return ev0.elapsed_time(ev1)
+
+
+def roofline_for(w, t_launch: float, o_size: int) -> dict:
+    """The roofline of one launch of `w` that took `t_launch` seconds: the
+    FFMA ALU rate for float32 (nominal), HBM for a step whose algorithmic
+    bytes take longer at the measured copy rate than its FLOPs at the bf16
+    peak, the tensor peak otherwise."""
+    peak, hbm_peak, peak_kind = load_peaks()
+    flops = w.flops()
+    achieved = flops / t_launch / 1e12
+    min_bytes = w.min_bytes(o_size)
+    if w.dtype == "f32":
+        return {"bound": "alu", "achieved": round(achieved, 4), "peak": FFMA_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": round(achieved / FFMA_PEAK_TFLOPS, 5),
+                "peak_source": FFMA_PEAK_SOURCE}
+    if min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
+        return {"bound": "hbm", "achieved": round(min_bytes / t_launch / 1e9, 1),
+                "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(min_bytes / t_launch / 1e9 / hbm_peak, 4),
+                "peak_source": f"hbm_gbs of {peak_kind}"}
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
+
+
+def bench_ours(args, w, rank, world, local):
+    import torch
+    import exact_attention_24_gb300 as fa
+    from exact_attention_24_gb300.build import build
+
+    build()
+    fa.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    run = FwdRunner(fa, w, dev, stream, rank_seed(w.seed, rank), args.splits)
+    q, k, v = run.host
+    f32, code, o_dtype, o_size = run.f32, run.code, run.o_dtype, run.o_size
 
     for i in range(args.warmup):
-        launch(i)
-    st = fa.fa_check_device_error(stream)
-    if st != fa.FA_OK:
-        raise fa.FaError(st, "warm-up")
+        run.launch(i)
+    run.check("warm-up")
 
-    sampler = ClockSampler(smi_gpu_id(local))
+    sampler = make_sampler(smi_gpu_id(local))
     sampler.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    sampler.mark()
-    ev0.record(stream)
-    for i in range(args.steps):
-        launch(i)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark()
-    barrier(world)
+    ms_local = run.timed(args.steps, sampler, world)
     sampler.stop()
-    st = fa.fa_check_device_error(stream)
-    if st != fa.FA_OK:
-        raise fa.FaError(st, "timed region")
-    ms_local = ev0.elapsed_time(ev1)
+    run.check("timed region")
     ms = reduce_max(ms_local, world, device=dev)
     per_step_ms = ms / args.steps
     flops = w.flops()
     value = world * flops * args.steps / (ms * 1e-3) / 1e12
-    achieved = flops / (ms_local / args.steps * 1e-3) / 1e12
 
     # ----------------------------------------------------------- e2e
     e2e_steps = max(3, min(args.steps, 30))
@@ -343,8 +500,8 @@ def bench_ours(args, w, rank, world, local):
     kh = k.pin_memory()
     vh = v.pin_memory()
     oh = torch.empty(q.shape, dtype=o_dtype).pin_memory()
-    lh = torch.empty(l_shape, dtype=torch.float32).pin_memory()
-    qd, kd, vd, O, L = bufs[0]
+    lh = torch.empty(run.l_shape, dtype=torch.float32).pin_memory()
+    qd, kd, vd, O, L = run.bufs[0]
 
     # A dense batch goes through fa_fwd_host: the public call for host
     # tensors, which overlaps the copies with the kernels run by run.  Other
@@ -362,7 +519,7 @@ def bench_ours(args, w, rank, world, local):
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
-            call(qd, kd, vd, O, L)
+            run.call(qd, kd, vd, O, L)
             oh.copy_(O, non_blocking=True)
             lh.copy_(L, non_blocking=True)
 
@@ -380,24 +537,9 @@ def bench_ours(args, w, rank, world, local):
     barrier(world)
     e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
-    peak, hbm_peak, peak_kind = load_peaks()
     min_bytes = w.min_bytes(o_size)
     t_launch = ms_local / args.steps * 1e-3
-    if f32:
-        # FFMA kernel: plain fp32 ALU arithmetic against the nominal FFMA rate
-        roofline = {"bound": "alu", "achieved": round(achieved, 4), "peak": FFMA_PEAK_TFLOPS,
-                    "unit": "TFLOP/s", "frac": round(achieved / FFMA_PEAK_TFLOPS, 5),
-                    "peak_source": FFMA_PEAK_SOURCE}
-    elif min_bytes / (hbm_peak * 1e9) > flops / (peak * 1e12):
-        roofline = {"bound": "hbm", "achieved": round(min_bytes / t_launch / 1e9, 1),
-                     "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(min_bytes / t_launch / 1e9 / hbm_peak, 4),
-                     "peak_source": f"hbm_gbs of {peak_kind}"}
-    else:
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2),
-                    "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4),
-                    "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
+    roofline = roofline_for(w, t_launch, o_size)
     roofline["traffic"] = load_traffic("fa_simt" if f32 else "fa_tc", w.name)
     rec = {
         "metric": METRIC,
@@ -418,8 +560,7 @@ def bench_ours(args, w, rank, world, local):
                    "lengths": list(w.lengths) if w.varlen else None,
                    "splits": args.splits,
                    "flops_per_step": flops,
-                   "l2": f"inputs rotated over {copies} resident copies "
-                         f"({copies * (in_bytes + out_b) / 1e6:.0f} MB > 129 MB L2)",
+                   "l2": run.l2_note,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
         "roofline": roofline,
         "io": {"min_bytes": min_bytes,
@@ -427,13 +568,113 @@ def bench_ours(args, w, rank, world, local):
                "tile_model_bytes": io_model_bytes(w, 256, 128),
                "tile_model_bytes_64x64": io_model_bytes(w, 64, 64)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
-                "h2d_bytes_per_step": in_bytes,
+                "h2d_bytes_per_step": run.in_bytes,
                 "d2h_bytes_per_step": oh.numel() * o_size + lh.numel() * 4,
                 "steps": e2e_steps,
                 "call": f"fa_fwd_host, {args.e2e_runs} runs" if host_api else "copies, then the call"},
-        "gpu_launches": args.steps * (2 if args.splits not in (None, 1) and ws_bytes else 1),
+        "gpu_launches": args.steps * run.launches_per_step,
         "clocks": sampler.summary(),
     }
+    # the default run (the headline workload on one GPU) also measures the
+    # other workloads, a seconds-long run of the headline, and the host link
+    if world == 1 and args.extras and w.name == HEADLINE and args.splits is None:
+        rec["e2e"]["host_link_gbs"] = host_link_rate(dev, stream)
+        del run
+        torch.cuda.empty_cache()
+        rec["per_config"] = per_config(fa, dev, stream, local, args)
+        rec["sustained"] = sustained(fa, w, dev, stream, local, args)
+    return rec
+
+
+def host_link_rate(dev, stream, nbytes: int = 256 << 20, reps: int = 5) -> dict:
+    """Raw pinned host <-> device copy rate on this machine (one 256 MiB copy at a
+    time, best of `reps`), the bound of the end-to-end leg's copies."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    out["bytes_per_copy"] = nbytes
+    return out
+
+
+def _timed_record(run, w, local, min_seconds: float, warmup: int) -> dict:
+    """Time `w` for at least `min_seconds` of device time (the step count is
+    sized from a short trial) with the clock sampler running, and return its
+    value, roofline and clocks."""
+    for i in range(warmup):
+        run.launch(i)
+    run.check("warm-up")
+    trial = run.timed(20)
+    steps = max(20, int(math.ceil(min_seconds / (trial / 20 * 1e-3))))
+    sampler = make_sampler(smi_gpu_id(local))
+    sampler.start()
+    ms = run.timed(steps, sampler)
+    sampler.stop()
+    run.check("timed region")
+    t_launch = ms / steps * 1e-3
+    roof = roofline_for(w, t_launch, run.o_size)
+    roof["traffic"] = load_traffic("fa_simt" if run.f32 else "fa_tc", w.name)
+    return {"value": round(w.flops() / t_launch / 1e12, 3), "unit": UNIT,
+            "ms_per_step": round(ms / steps, 5), "steps": steps,
+            "achieved_hbm_gbs": round(w.min_bytes(run.o_size) / t_launch / 1e9, 1),
+            "roofline": roof, "l2": run.l2_note,
+            "gpu_launches": steps * run.launches_per_step, "clocks": sampler.summary()}
+
+
+def per_config(fa, dev, stream, local, args) -> dict:
+    """The other benchmark workloads (C1, C2, C4, C5), each timed the way the
+    headline is, for at least `--config-seconds` of device time so that the
+    clock sampler sees the timed region."""
+    import torch
+    from exact_attention_24_gb300.workloads import C1, C2, C4, C5
+    out = {}
+    for w in (C1, C2, C4, C5):
+        run = FwdRunner(fa, w, dev, stream, w.seed)
+        rec = _timed_record(run, w, local, args.config_seconds, args.warmup)
+        rec["config"] = {"B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                         "dtype": w.dtype, "seed": w.seed,
+                         "lengths": list(w.lengths) if w.varlen else None}
+        out[w.name] = rec
+        del run
+        torch.cuda.empty_cache()
+    return out
+
+
+def sustained(fa, w, dev, stream, local, args) -> dict:
+    """The headline workload repeated for at least `--sustained-seconds` of
+    timed device time: its rate once clocks have settled under load, against
+    the sustained bf16 peak, with the clock seen and time x clock (the cycles
+    a step takes), so that clock dependence shows."""
+    import torch
+    run = FwdRunner(fa, w, dev, stream, w.seed)
+    rec = _timed_record(run, w, local, args.sustained_seconds, args.warmup)
+    del run
+    torch.cuda.empty_cache()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sus_peak, kind = float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        sus_peak, kind = 1700.0, "fallback"
+    mhz = (rec["clocks"] or {}).get("sm_mhz")
+    rec["frac_of_sustained_peak"] = round(rec["value"] / sus_peak, 4)
+    rec["sustained_peak"] = {"value": sus_peak, "unit": UNIT,
+                             "source": f"bf16_tflops_sustained of {kind}"}
+    if mhz:
+        rec["mcycles_per_step"] = round(rec["ms_per_step"] * mhz / 1e3, 4)
+        rec["tflops_per_ghz"] = round(rec["value"] / (mhz / 1e3), 2)
+    rec["workload"] = w.name
     return rec
 
 
@@ -509,7 +750,7 @@ def bench_bwd(args, w, rank, world, local):
     st = fa.fa_check_device_error(stream)
     if st != fa.FA_OK:
         raise fa.FaError(st, "warm-up")
-    sampler = ClockSampler(smi_gpu_id(local))
+    sampler = make_sampler(smi_gpu_id(local))
     sampler.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -868,7 +1109,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="B2_H16_N4096_D128_bf16_causal")
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0 = leave it out)")
     ap.add_argument("--splits", type=int, default=None,
@@ -887,6 +1128,12 @@ def main(argv=None):
                     help="runs that fa_fwd_host cuts a dense batch into for the e2e measurement")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="seconds of oracle time that --impl reference spreads over its steps")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="leave out per_config, sustained and the host-link rate (N=1 runs)")
+    ap.add_argument("--config-seconds", type=float, default=0.4,
+                    help="minimum timed device seconds of each per_config workload")
+    ap.add_argument("--sustained-seconds", type=float, default=2.5,
+                    help="minimum timed device seconds of the sustained leg")
     ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.cpu_one_core:

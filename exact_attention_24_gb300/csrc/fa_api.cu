@@ -1,6 +1,8 @@
 // C-ABI layer: argument validation, kernel selection, the device error word
 // and the watchdog self-test.  Declarations and contracts live in
 // include/fa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -20,30 +22,53 @@ namespace {
 
 fa_options g_opts = {FA_KERNEL_AUTO, 0, 0};
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kMaxDevices = 64;
-uint32_t *g_err_addr[kMaxDevices];
-std::mutex g_err_mu;
 
-// Device address of the error word on the current device (looked up once
-// per device; the host-side symbol is not a device address).
+// A small table from CUDA context id (fa_context_id) to a value that
+// belongs to that context; thread-safe.  When full, the oldest entry makes
+// room (its context only repeats the lookup).
+template <typename T>
+struct CtxTable {
+    static constexpr int kCap = 16;
+    std::mutex mu;
+    uint64_t ids[kCap] = {};
+    T vals[kCap] = {};
+    int next = 0;
+    bool get(uint64_t id, T &out) {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < kCap; ++i)
+            if (id && ids[i] == id) {
+                out = vals[i];
+                return true;
+            }
+        return false;
+    }
+    void put(uint64_t id, const T &v) {
+        if (!id) return;
+        std::lock_guard<std::mutex> lk(mu);
+        ids[next] = id;
+        vals[next] = v;
+        next = (next + 1) % kCap;
+    }
+};
+
+CtxTable<uint32_t *> g_err_addr;
+
+// Device address of the error word in the current context.  In host code
+// the symbol names a host-side stand-in, so the runtime is asked for the
+// address (which also creates the context if none is current yet), once per
+// context.
 uint32_t *err_word() {
-    int dev = 0;
-    const cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    const uint64_t id = fa_context_id();
+    uint32_t *addr = nullptr;
+    if (g_err_addr.get(id, addr)) return addr;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_error_word);
+    if (e != cudaSuccess) {
+        fa_cuda_fail(e);
         return nullptr;
     }
-    std::lock_guard<std::mutex> lk(g_err_mu);
-    if (!g_err_addr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_error_word);
-        if (e != cudaSuccess) {
-            fa_cuda_fail(e);
-            return nullptr;
-        }
-        g_err_addr[dev] = static_cast<uint32_t *>(p);
-    }
-    return g_err_addr[dev];
+    g_err_addr.put(id ? id : fa_context_id(), static_cast<uint32_t *>(p));
+    return static_cast<uint32_t *>(p);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -53,28 +78,39 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-// fa_fwd_host's copy streams and run events, created on a device's first call
-// and kept for the process; g_pipe_mu also serialises the enqueueing.
+// fa_fwd_host's copy streams and run events, created in a context on its
+// first call there and kept for the process; g_pipe_mu also serialises the
+// enqueueing.
 constexpr int kMaxHostChunks = 64;
 struct HostPipe {
-    bool ready = false;
+    uint64_t ctx = 0;
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
     cudaEvent_t landed[kMaxHostChunks], computed[kMaxHostChunks];
 };
-HostPipe g_pipes[kMaxDevices];
+constexpr int kMaxPipes = 16;
+HostPipe g_pipes[kMaxPipes];
+int g_pipes_used = 0;
 std::mutex g_pipe_mu;
 
-// The current device's pipe (g_pipe_mu held), or null after recording the failure.
+// The current context's pipe (g_pipe_mu held), or null after recording the
+// failure.
 HostPipe *host_pipe() {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        fa_cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    // the error word's lookup makes sure a context is current
+    if (!err_word()) return nullptr;
+    const uint64_t id = fa_context_id();
+    if (!id) {
+        fa_cuda_fail(cudaErrorDeviceUninitialized);
         return nullptr;
     }
-    HostPipe &hp = g_pipes[dev];
-    if (hp.ready) return &hp;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < g_pipes_used; ++i)
+        if (g_pipes[i].ctx == id) return &g_pipes[i];
+    if (g_pipes_used == kMaxPipes) {
+        fa_cuda_fail(cudaErrorNotSupported);
+        return nullptr;
+    }
+    HostPipe hp;
     const unsigned ev = cudaEventDisableTiming;
     e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
@@ -88,8 +124,9 @@ HostPipe *host_pipe() {
         fa_cuda_fail(e);
         return nullptr;
     }
-    hp.ready = true;
-    return &hp;
+    hp.ctx = id;
+    g_pipes[g_pipes_used] = hp;
+    return &g_pipes[g_pipes_used++];
 }
 
 size_t in_bytes(int dtype) { return dtype == FA_F32 ? 4 : 2; }
@@ -122,21 +159,24 @@ fa_status check_common(const void *Q, const void *K, const void *V, void *O, flo
     return FA_OK;
 }
 
+// Kernel choice.  bf16 runs on the tensor-core kernel: a bf16 case that
+// kernel cannot take is reported to the caller as FA_ERR_UNSUPPORTED, before
+// any CUDA call, and never handed to the FFMA kernel in its place.  The FFMA
+// kernel serves float32, and bf16 only when the caller asks for it
+// (FA_KERNEL_SIMT).
 fa_status dispatch(FaProblem &p) {
+    const bool bf16 = p.dtype != FA_F32;
+    const bool simt = g_opts.kernel == FA_KERNEL_SIMT || (g_opts.kernel == FA_KERNEL_AUTO && !bf16);
+    if (!simt) {
+        if (!bf16) return FA_ERR_UNSUPPORTED;
+        const fa_status st = fa_tc_supports(p);
+        if (st != FA_OK) return st;
+    }
     p.err = err_word();
     if (!p.err) return FA_ERR_CUDA;
     p.grid_ctas = g_opts.grid_ctas;
     p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
-    const bool bf16 = p.dtype != FA_F32;
-    switch (g_opts.kernel) {
-        case FA_KERNEL_SIMT: return fa_launch_simt(p);
-        case FA_KERNEL_TC: return bf16 ? fa_launch_tc(p) : FA_ERR_UNSUPPORTED;
-        default: {
-            if (!bf16) return fa_launch_simt(p);
-            const fa_status st = fa_launch_tc(p);
-            return st == FA_ERR_UNSUPPORTED ? fa_launch_simt(p) : st;
-        }
-    }
+    return simt ? fa_launch_simt(p) : fa_launch_tc(p);
 }
 
 __global__ void watchdog_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
@@ -164,6 +204,36 @@ fa_status fa_cuda_fail(cudaError_t e) {
     t_last_cuda_error = e;
     cudaGetLastError();
     return FA_ERR_CUDA;
+}
+
+uint64_t fa_context_id() {
+    // cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points
+    // (the library links the runtime only), looked up once
+    struct Fns {
+        PFN_cuCtxGetCurrent_v4000 current = nullptr;
+        PFN_cuCtxGetId_v12000 id = nullptr;
+    };
+    static const Fns fns = []() {
+        Fns f;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        cudaGetLastError();
+        return f;
+    }();
+    if (!fns.current || !fns.id) return 0;
+    CUcontext ctx = nullptr;
+    if (fns.current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (fns.id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
 }
 
 fa_status fa_launch_watchdog_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t s) {
@@ -419,22 +489,23 @@ static fa_status check_bwd(const void *Q, const void *K, const void *V, const vo
     return FA_OK;
 }
 
+// Kernel choice as in dispatch: bf16 gradients come from the tensor-core
+// kernels or the call returns the reason they cannot, before any launch.
 static fa_status run_bwd(FaBwdProblem &p) {
+    const bool bf16 = p.dtype != FA_F32;
+    const bool simt = g_opts.kernel == FA_KERNEL_SIMT || (g_opts.kernel == FA_KERNEL_AUTO && !bf16);
+    if (!simt) {
+        if (!bf16) return FA_ERR_UNSUPPORTED;
+        const fa_status st = fa_bwd_tc_supports(p);
+        if (st != FA_OK) return st;
+    }
     p.err = err_word();
     if (!p.err) return FA_ERR_CUDA;
     p.grid_ctas = g_opts.grid_ctas;
     p.wait_limit_ns = g_opts.wait_limit_ns ? g_opts.wait_limit_ns : kDefaultWaitLimitNs;
     fa_status st = fa_launch_bwd_delta(p);
     if (st != FA_OK) return st;
-    const bool bf16 = p.dtype != FA_F32;
-    switch (g_opts.kernel) {
-        case FA_KERNEL_SIMT: return fa_launch_bwd_simt(p);
-        case FA_KERNEL_TC: return bf16 ? fa_launch_bwd_tc(p) : FA_ERR_UNSUPPORTED;
-        default:
-            if (!bf16) return fa_launch_bwd_simt(p);
-            st = fa_launch_bwd_tc(p);
-            return st == FA_ERR_UNSUPPORTED ? fa_launch_bwd_simt(p) : st;
-    }
+    return simt ? fa_launch_bwd_simt(p) : fa_launch_bwd_tc(p);
 }
 
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,

@@ -866,8 +866,8 @@ fa_status launch(const FaBwdProblem &p) {
     k.wait_limit_ns = p.wait_limit_ns;
     const long long grid = (long long)k.nblk * p.units_bh;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
-    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
-    const fa_status su = fa_once_per_device(ready, []() -> fa_status {
+    static FaCtxSet ready;  // contexts set up for this instantiation
+    const fa_status su = fa_once_per_context(ready, []() -> fa_status {
         const fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes);
         return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes) : st;
     });
@@ -887,8 +887,18 @@ fa_status launch(const FaBwdProblem &p) {
 }  // namespace
 }  // namespace fa
 
+fa_status fa_bwd_tc_supports(const FaBwdProblem &p) {
+    if (p.dtype != FA_BF16 && p.dtype != FA_BF16_OUT_F32) return FA_ERR_UNSUPPORTED;
+    if (p.D != 64 && p.D != 128) return FA_ERR_UNSUPPORTED;
+    // one CTA-sized block per 128 keys (or rows) of every problem, counted in 32 bits
+    if (p.n < 0 || p.units_bh < 0 || (int64_t)((p.n + fa::kT - 1) / fa::kT) * p.units_bh > INT32_MAX)
+        return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
 fa_status fa_launch_bwd_tc(const FaBwdProblem &p) {
-    if (p.dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+    const fa_status sup = fa_bwd_tc_supports(p);
+    if (sup != FA_OK) return sup;
     if ((int64_t)p.units_bh * p.n == 0) return FA_OK;
     const bool f32 = p.dtype == FA_BF16_OUT_F32;
     // the band instantiation serves windows other than causal (-1, 0) and full (-1, -1)

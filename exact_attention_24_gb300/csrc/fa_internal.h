@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "../../include/fa.h"
 
@@ -70,20 +71,51 @@ struct FaBwdProblem {
 // Returns FA_ERR_CUDA so launchers can `return fa_cuda_fail(e);`.
 fa_status fa_cuda_fail(cudaError_t e);
 
+// Unique id of the CUDA context current on the calling thread -- the one the
+// runtime's next call uses -- or 0 if there is none yet (or the driver cannot
+// say).  Device addresses of module globals and kernel attributes belong to
+// a context, not to a device number: a context made after cudaDeviceReset,
+// or a host program's own driver-API context, loads this library's module
+// afresh.  Every cache of such values is keyed by this id.
+uint64_t fa_context_id();
+
+// A small set of context ids (see fa_context_id), thread-safe.  When full,
+// the oldest entry makes room: a forgotten context only repeats its set-up.
+struct FaCtxSet {
+    static constexpr int kCap = 16;
+    std::mutex mu;
+    uint64_t ids[kCap] = {};
+    int next = 0;
+    bool has(uint64_t id) {
+        std::lock_guard<std::mutex> lk(mu);
+        for (uint64_t x : ids)
+            if (x == id) return true;
+        return false;
+    }
+    void add(uint64_t id) {
+        std::lock_guard<std::mutex> lk(mu);
+        for (uint64_t x : ids)
+            if (x == id) return;
+        ids[next] = id;
+        next = (next + 1) % kCap;
+    }
+};
+
 // Run `setup` (kernel attributes: dynamic shared memory and the like) once
-// per device and kernel instantiation; `done` is that instantiation's mask
-// of devices already set up.  Launches after the first then make no runtime
-// calls besides the launch itself, so they can also be captured in a CUDA
-// graph.  Returns the first failure of `setup`, which is retried next time.
+// per CUDA context and kernel instantiation; `done` is that instantiation's
+// set of contexts already set up.  Launches after the first then make no
+// runtime calls besides the launch itself, so they can also be captured in a
+// CUDA graph.  Returns the first failure of `setup`, which is retried next
+// time.
 template <typename F>
-inline fa_status fa_once_per_device(std::atomic<uint64_t> &done, F &&setup) {
-    int dev = 0;
-    const cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fa_cuda_fail(e);
-    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
-    if (bit && (done.load(std::memory_order_acquire) & bit)) return FA_OK;
-    const fa_status st = setup();
-    if (st == FA_OK && bit) done.fetch_or(bit, std::memory_order_release);
+inline fa_status fa_once_per_context(FaCtxSet &done, F &&setup) {
+    const uint64_t id = fa_context_id();
+    if (id && done.has(id)) return FA_OK;
+    const fa_status st = setup();  // its runtime calls create the context if need be
+    if (st == FA_OK) {
+        const uint64_t now = id ? id : fa_context_id();
+        if (now) done.add(now);
+    }
     return st;
 }
 
@@ -115,6 +147,11 @@ fa_status fa_launch_bwd_delta(const FaBwdProblem &p);
 fa_status fa_launch_bwd_simt(const FaBwdProblem &p);
 fa_status fa_launch_bwd_tc(const FaBwdProblem &p);
 fa_status fa_launch_tc(const FaProblem &p);
+// What the tensor-core launchers accept, decided on the host without any
+// CUDA call: FA_OK, or FA_ERR_UNSUPPORTED for a dtype, head dimension, mode
+// or size they do not take.
+fa_status fa_tc_supports(const FaProblem &p);
+fa_status fa_bwd_tc_supports(const FaBwdProblem &p);
 
 // Split-key planning for the tensor-core kernel: the number of key-range
 // splits used for `requested` (0 = automatic: enough work items to cover the

@@ -20,27 +20,37 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRA
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices];
+constexpr int kMaxContexts = 16;
+uint64_t g_scratch_ctx[kMaxContexts];
+void *g_scratch_addr[kMaxContexts];
+int g_scratch_next = 0;
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device.  In host code
-// `g_noalloc_scratch` names a host-side stand-in, not device memory, so the
-// runtime is asked for the address -- once per device, on the first call
-// made with that device current -- and the address is what the kernels get.
+// Device address of the scratch array in the current CUDA context.  In host
+// code `g_noalloc_scratch` names a host-side stand-in, not device memory, so
+// the runtime is asked for the address -- once per context, on the first
+// call made with that context current -- and the address is what the kernels
+// get.  The address belongs to the context, not to the device number: a
+// context made later (after cudaDeviceReset, or a host program's own
+// driver-API context) loads the module afresh and gets its own lookup.
 fa_status scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fa_cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    const uint64_t id = fa_context_id();
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return fa_cuda_fail(e);
-        g_scratch_addr[dev] = p;
+    for (int i = 0; id && i < kMaxContexts; ++i)
+        if (g_scratch_ctx[i] == id) {
+            *out = g_scratch_addr[i];
+            return FA_OK;
+        }
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // creates the context if needed
+    if (e != cudaSuccess) return fa_cuda_fail(e);
+    const uint64_t now = id ? id : fa_context_id();
+    if (now) {
+        g_scratch_ctx[g_scratch_next] = now;
+        g_scratch_addr[g_scratch_next] = p;
+        g_scratch_next = (g_scratch_next + 1) % kMaxContexts;
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return FA_OK;
 }
 

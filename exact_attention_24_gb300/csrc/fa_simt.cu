@@ -231,8 +231,8 @@ fa_status launch(const FaProblem &pr) {
     p.err = pr.err;
     const size_t smem = sizeof(float) * (size_t)(kBr * D + kBc * (D + 1) + kBc * D);
     auto kern = fa_simt_kernel<D, RPW, Tin, Tout>;
-    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
-    const fa_status su = fa_once_per_device(ready, [&]() -> fa_status {
+    static FaCtxSet ready;  // contexts set up for this instantiation
+    const fa_status su = fa_once_per_context(ready, [&]() -> fa_status {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
     });

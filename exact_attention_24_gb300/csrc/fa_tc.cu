@@ -1020,8 +1020,8 @@ fa_status launch(const FaProblem &pr, int splits) {
     if (grid <= 0) return FA_ERR_CUDA;  // device query failed (recorded)
     if (grid > p.num_items) grid = p.num_items;
     auto kern = fa_tc_kernel<D, OUT, WIN>;
-    static std::atomic<uint64_t> ready{0};  // devices set up for this instantiation
-    const fa_status su = fa_once_per_device(ready, [&]() -> fa_status {
+    static FaCtxSet ready;  // contexts set up for this instantiation
+    const fa_status su = fa_once_per_context(ready, [&]() -> fa_status {
         cudaFuncAttributes fattr;
         cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
         if (e != cudaSuccess) return fa_cuda_fail(e);
@@ -1100,9 +1100,20 @@ bool fa_tc_split_plan(int units_bh, int n, int D, int requested, int &splits, si
     return true;
 }
 
-fa_status fa_launch_tc(const FaProblem &pr) {
+fa_status fa_tc_supports(const FaProblem &pr) {
     if (pr.dtype != FA_BF16 && pr.dtype != FA_BF16_OUT_F32) return FA_ERR_UNSUPPORTED;
     if (pr.num_splits > 1 && (pr.varlen || pr.wl >= 0 || pr.wr > 0)) return FA_ERR_UNSUPPORTED;
+    if (pr.D != 64 && pr.D != 128) return FA_ERR_UNSUPPORTED;
+    // work items are numbered in 32-bit arithmetic with headroom
+    const int64_t items = (int64_t)((pr.n + 2 * fa::BM - 1) / (2 * fa::BM)) *
+                          (pr.num_splits > 1 ? pr.num_splits : 1) * pr.units_bh;
+    if (pr.n < 0 || pr.units_bh < 0 || items > INT32_MAX / 2) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status fa_launch_tc(const FaProblem &pr) {
+    const fa_status sup = fa_tc_supports(pr);
+    if (sup != FA_OK) return sup;
     if (pr.D == 64) return fa::launch_d<64>(pr);
     if (pr.D == 128) return fa::launch_d<128>(pr);
     return FA_ERR_UNSUPPORTED;

@@ -196,9 +196,11 @@ FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int D,
  *  - Sizes whose split workspace (fa_fwd_splitkv_workspace_size) exceeds
  *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED before
  *    anything is enqueued.
- *  - The first call on a device looks up the array's device address (a
- *    runtime query, no allocation) with that device current; make that first
- *    call before any stream capture on the device.
+ *  - The first call in a CUDA context looks up the array's device address
+ *    there (a runtime query, no allocation); make that first call before any
+ *    stream capture in the context.  The address belongs to the context: a
+ *    new context (after cudaDeviceReset, or a host program's own driver-API
+ *    context made current) gets its own lookup on its first call.
  *  - All calls share the array: calls that overlap on the GPU (other
  *    streams, other host threads) race on it.  Order them on one stream.
  */
@@ -362,7 +364,10 @@ FA_API const char *fa_last_cuda_error(void);
  * concurrent fa_fwd calls).
  *
  *   kernel        : FA_KERNEL_AUTO picks the tensor-core kernel for the
- *                   bf16 dtypes and the FFMA kernel for FA_F32;
+ *                   bf16 dtypes and the FFMA kernel for FA_F32; a bf16
+ *                   problem the tensor-core kernel cannot take returns
+ *                   FA_ERR_UNSUPPORTED (decided before any CUDA call) and
+ *                   is never run on the FFMA kernel instead;
  *                   FA_KERNEL_SIMT forces the FFMA kernel for every dtype;
  *                   FA_KERNEL_TC forces the tensor-core kernel (bf16 only,
  *                   FA_ERR_UNSUPPORTED otherwise).

@@ -133,6 +133,40 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     assert fa.fa_check_device_error(0) == fa.FA_ERR_CUDA
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake addresses are for GPU-less hosts only")
+def test_bf16_case_the_tensor_cores_cannot_take_is_reported(lib):
+    """A bf16 problem the tensor-core kernels do not take (here: more work
+    items than their 32-bit numbering allows) returns FA_ERR_UNSUPPORTED to
+    the caller, decided on the host before any CUDA call -- it is never run on
+    the FFMA kernel instead.  Without a GPU, any CUDA call would have turned
+    the result into FA_ERR_CUDA."""
+    far = [(i + 1) << 47 for i in range(10)]   # fake, far apart: nothing overlaps
+    q, k, v, o, l = far[:5]
+    H, N = 1 << 22, 1 << 16                   # 256 blocks x 2^22 heads = 2^30 items
+    for kernel in (fa.FA_KERNEL_AUTO, fa.FA_KERNEL_TC):
+        assert fa.fa_set_options(kernel, 0, 0) == fa.FA_OK
+        try:
+            for code in (fa.FA_BF16, fa.FA_BF16_OUT_F32):
+                for causal in (0, 1):
+                    assert fa.fa_fwd(q, k, v, o, l, 1, H, N, 64, 0.1, causal, code, 0) == \
+                        fa.FA_ERR_UNSUPPORTED
+            # backward: 2^11 key blocks x 2^20 heads = 2^31 blocks
+            Hb, Nb = 1 << 20, 1 << 18
+            nws = fa.fa_bwd_workspace_size(1, Hb, Nb)
+            assert fa.fa_bwd(*far[:9], 1, Hb, Nb, 64, 0.1, 1, fa.FA_BF16, far[9], nws, 0) == \
+                fa.FA_ERR_UNSUPPORTED
+            # one item fewer is taken (and, with no GPU, then fails in CUDA)
+            assert fa.fa_fwd(q, k, v, o, l, 1, H - 1, N, 64, 0.1, 1, fa.FA_BF16, 0) == fa.FA_ERR_CUDA
+        finally:
+            fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+    # float32 never reaches the tensor-core kernel
+    assert fa.fa_set_options(fa.FA_KERNEL_TC, 0, 0) == fa.FA_OK
+    try:
+        assert fa.fa_fwd(q, k, v, o, l, 1, 1, 16, 64, 0.1, 0, fa.FA_F32, 0) == fa.FA_ERR_UNSUPPORTED
+    finally:
+        fa.fa_set_options(fa.FA_KERNEL_AUTO, 0, 0)
+
+
 def test_product_package_does_not_import_oracle():
     """The oracle is test infrastructure: nothing in the product package may
     import or load it."""

@@ -1,7 +1,9 @@
 """The library from plain C: a C program (tests/c_abi/abi_demo.c) built with
 gcc against include/fa.h and the shared library, allocating its own device
-memory with the CUDA runtime, runs fa_fwd and fa_bwd in float32; its outputs
-are compared here with the float64 oracle.  No torch on that path."""
+memory with the CUDA runtime, runs fa_fwd and fa_bwd in float32 (the FFMA
+kernels), and in a second mode fa_fwd on bf16 inputs on the tensor-core
+kernel; its outputs are compared here with the float64 oracle.  No torch on
+that path."""
 
 import os
 import shutil
@@ -14,6 +16,7 @@ import torch
 import exact_attention_24_gb300 as fa
 from exact_attention_24_gb300 import build as fa_build
 from exact_attention_24_gb300.workloads import Workload, make_inputs
+from helpers import assert_close
 from oracle import attention_bwd_ref, attention_ref
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -60,3 +63,27 @@ def test_c_program_matches_oracle(tmp_path):
     assert np.max(np.abs(O - ref_o)) <= 1e-4 and np.max(np.abs(L - ref_l)) <= 1e-5
     for g, ref in zip((dq, dk, dv), attention_bwd_ref(q, k, v, do, w.scale, causal)[:3]):
         assert np.max(np.abs(g - ref)) <= 1e-4 * max(1.0, float(np.max(np.abs(ref))))
+
+
+@pytest.mark.gpu
+def test_c_program_tensor_core_bf16_matches_oracle(tmp_path):
+    """bf16 inputs on the tensor-core kernel from C: fp32 O and bf16 O, each
+    with L, against the oracle on the same bf16-rounded inputs."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    exe = _compile(tmp_path)
+    B, H, N, D, causal = 2, 2, 333, 128, True
+    w = Workload("c_abi_bf16", B, H, N, D, "bf16", causal, 9)
+    q, k, v = make_inputs(w)      # bf16 values: exact in the float32 file
+    inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
+    np.concatenate([x.float().numpy().ravel() for x in (q, k, v, q)]).astype(np.float32).tofile(inp)
+    r = subprocess.run([exe, str(inp), str(out), str(B), str(H), str(N), str(D), str(int(causal)),
+                        repr(w.scale), "bf16"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = np.fromfile(out, dtype=np.float32).astype(np.float64)
+    e, rows = B * H * N * D, B * H * N
+    o32, l1 = got[:e].reshape(B, H, N, D), got[e:e + rows].reshape(B, H, N)
+    o16, l2 = got[e + rows:2 * e + rows].reshape(B, H, N, D), got[2 * e + rows:].reshape(B, H, N)
+    ref_o, ref_l = attention_ref(q, k, v, w.scale, causal)
+    assert_close(o32, l1, ref_o, ref_l, fa.FA_BF16_OUT_F32, "C caller, fp32 O")
+    assert_close(o16, l2, ref_o, ref_l, fa.FA_BF16, "C caller, bf16 O")

@@ -4,8 +4,9 @@ that owns the device-memory budget, a latency-critical caller that must not
 call cudaMalloc/cudaFree, C code handed only its buffers).
 
 Two calls in a row, each through the C ABI, checked against the existing
-fa_fwd_splitkv (which takes a caller workspace) on the same inputs, with the
-parity tolerances of the other GPU tests.  Collected last on purpose.
+fa_fwd_splitkv (which takes a caller workspace) on the same inputs, and on
+sampled rows against the float64 oracle, with the parity tolerances of the
+other GPU tests.  Collected last on purpose.
 """
 
 import numpy as np
@@ -15,7 +16,8 @@ import torch
 import exact_attention_24_gb300 as fa
 from exact_attention_24_gb300 import build as fa_build
 from exact_attention_24_gb300.workloads import Workload, make_inputs
-from helpers import TOL, half_ulp_bf16, to_f64
+from helpers import TOL, assert_close, half_ulp_bf16, sample_rows, to_f64
+from oracle import attention_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -73,12 +75,21 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         (Workload("b", 2, 1, 1500, 64, "bf16", False, 22), fa.FA_BF16_OUT_F32, 3),
     ]
     for w, code, splits in cases:   # two different calls in a row
-        assert fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.D, splits) <= \
-            fa.FA_NOALLOC_SCRATCH_BYTES
-        q, k, v = (x.to(DEV) for x in make_inputs(w))
+        need = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.D, splits)
+        # more than one split, so both calls really go through their scratch
+        assert 0 < need <= fa.FA_NOALLOC_SCRATCH_BYTES
+        qh, kh, vh = make_inputs(w)
+        q, k, v = qh.to(DEV), kh.to(DEV), vh.to(DEV)
         ref = _with_workspace(q, k, v, w, code, splits)
         got = _noalloc(q, k, v, w, code, splits)
         _check(got, ref, code, f"{w.name} splits={splits}")
+        # and against the float64 oracle on sampled rows of every head
+        for b in range(w.B):
+            for h in range(w.H):
+                rows = sample_rows(w.N, 24, seed=31 * b + h)
+                ro, rl = attention_rows(qh[b, h], kh[b, h], vh[b, h], w.scale, w.causal, rows)
+                assert_close(to_f64(got[0][b, h, rows]), to_f64(got[1][b, h, rows]), ro, rl, code,
+                             f"{w.name} b={b} h={h} vs oracle")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
