@@ -79,6 +79,15 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
                  : "memory");
 }
 
+// Named barrier `id` of `n` threads (whole warps): wait for it / arrive on
+// it without waiting.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel in
 // the stream (if launched with programmatic stream serialization) start its
 // CTAs as this grid's CTAs retire; wait blocks until every prerequisite grid

@@ -10,14 +10,15 @@
 // "Write the data back to HBM").  Work units are independent (the section
 // "Same operations in another block"), so a persistent grid walks them.
 //
-// How it maps onto GB300 (one CTA per SM, 10 warps):
+// How it maps onto GB300 (one CTA per SM, 11 warps):
 //   warps 0-3  softmax for query tile 0 (rows 0..127 of the CTA's block;
 //              TMEM lanes 0..127, one row per thread)
 //   warps 4-7  softmax for query tile 1 (rows 128..255)
 //   warp 8     TMA producer: Q tiles once per block, then K_j, V_j tiles
 //              through an NSLOT-deep ring of shared-memory slots guarded by
 //              full/empty mbarriers
-//   warp 9     TMEM allocator and MMA issuer (one thread):
+//   warps 9-10 MMA issuers, one per query tile s (one elected thread each;
+//              warp 9 also allocates TMEM), taking turns through a token:
 //                S_s = Q_s K_j^T          tcgen05.mma, A and B in smem
 //                O_s (+)= P_s V_j         tcgen05.mma, A (=P, bf16) in TMEM
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
@@ -49,9 +50,11 @@ namespace {
 
 constexpr int BM = 128;             // rows per query tile (MMA M)
 constexpr int BN = 128;             // keys per K/V tile
-constexpr int kThreads = 320;       // 10 warps
+constexpr int kThreads = 352;       // 11 warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarpA = 9;        // MMA issuer of query tile 0; allocates TMEM
+constexpr int kMmaWarpB = 10;       // MMA issuer of query tile 1
+constexpr uint32_t kTokenBar = 1;   // named barriers 1, 2: the issuers' turn tokens
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 16.0f;  // log2 units
 // Epilogue destinations.
@@ -305,7 +308,7 @@ __device__ __forceinline__ bool decode_item(const TcParams &p, const Sched &sc, 
 
 // --------------------------------------------------------------- kernel --
 template <int D, int OUT, bool WIN>
-// 10 warps put 3 warps on two of the four SM sub-partitions, whose register
+// 11 warps put 3 warps on three of the four SM sub-partitions, whose register
 // files hold 16K registers each: at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
     fa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gbars = gbase + C::kBarOff;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + C::kBarBytes - 8);
+    volatile int *exit_flag = reinterpret_cast<volatile int *>(gbars + C::kBarBytes - 12);  // issuers stop
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Band masks with a left bound exist only in the WIN instantiation; the
@@ -343,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     if (warp == kProducerWarp && lane == 0) {
         mbar_init(bar_q_full, 1);
-        mbar_init(bar_q_empty, 1);
+        mbar_init(bar_q_empty, 2);    // one commit per issuer warp
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(bar_kv_full + 8 * i, 1);
-            mbar_init(bar_kv_empty + 8 * i, 1);
+            mbar_init(bar_kv_empty + 8 * i, 2);   // one commit per issuer warp
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_s_full + 8 * s, 1);
@@ -355,14 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_s_free + 8 * s, 4);
             mbar_init(bar_pv_done + 8 * s, 1);
         }
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, 2);
         *abort_flag = 0;
+        *exit_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarpA) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -468,223 +473,169 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain(bar_kv_full + 8 * (i % C::kSlots), (i / C::kSlots) & 1, lim);
             if (items > 0) mbar_drain(bar_q_full, (items - 1) & 1, lim);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
         // ----------------------------------------------------------- MMA
-        // The whole warp runs this role's control flow and waits; one elected
-        // lane issues every tcgen05.mma / commit (always the same lane).
-        const uint64_t dq0 = smem_desc(q_smem, 16, 1024);
-        const uint64_t dq1 = smem_desc(q_smem + C::kTileBytes, 16, 1024);
+        // Two issuer warps, one per query tile s.  tcgen05.mma issue is
+        // effectively synchronous with execution, so every cycle an issuer
+        // spends on barrier waits, commits and control is tensor idle time.
+        // The warps therefore take turns: each does its waits while the other
+        // is issuing, then takes the turn token (a named barrier the other
+        // warp arrives on when its block is issued) and issues its own block
+        // back to back.  The token keeps the two tiles' blocks from
+        // interleaving, so each block completes as early as with one issuer.
+        // Within a warp the whole warp runs the control flow and waits; one
+        // elected lane issues every tcgen05.mma / commit (always the same
+        // lane).  A ring slot is released by both warps (its empty barrier
+        // counts two commits), each commit covering that warp's reads of it.
+        const int s = warp - kMmaWarpA;    // query tile this warp issues for
+        const uint64_t dq_s = smem_desc(q_smem + s * C::kTileBytes, 16, 1024);
         const uint64_t dk_ring = smem_desc(ring, 16, 1024);
         const uint64_t dv_ring = smem_desc(ring, C::kHalfBytes, 1024);
         constexpr uint64_t kSlotDesc = C::kTileBytes >> 4;  // one slot in descriptor units
-        const uint32_t t_s0 = tmem, t_s1 = tmem + BN;
-        const uint32_t t_o0 = tmem + 2 * BN, t_o1 = tmem + 2 * BN + D;
-        uint32_t lc = 0, items = 0, pc0 = 0, pc1 = 0, fc0 = 0, fc1 = 0;
-        bool ok = true;
-        if (!C::kPAlias) {
-            // D=64: P_s has its own TMEM columns.  Per K/V tile j: both next
-            // Q K^T as soon as the softmaxes have read S(j), then both P V.
-            const uint32_t t_p0 = tmem + 2 * BN + 2 * D, t_p1 = t_p0 + BN / 2;
-            for (int k = 0; ok && k * G < p.num_items; ++k) {
-                const int idx = snake_item(k, cta, G);
-                if (idx >= p.num_items) continue;
-                Item it;
-                if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
-                if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
-                ++items;
-                tc_fence_after();
-                const uint32_t l0 = lc;
-                lc += 2 * it.nkv;
-                if (!ring_wait(bar_kv_full, l0, C::kSlots, wc, 4)) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
-                    const uint64_t dk0 = dk_ring + (l0 % C::kSlots) * kSlotDesc;
-                    // Query tile 0's range starts at t0; in split mode it can be
-                    // empty (the last key range of a short causal block).
-                    if (it.nk0 > 0) {
-                        issue_qk<D>(t_s0, dq0, dk0);
-                        mma_commit(bar_s_full);
-                    }
-                    if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
-                        issue_qk<D>(t_s1, dq1, dk0);
-                        mma_commit(bar_s_full + 8);
-                    }
-                    mma_commit(bar_kv_empty + 8 * (l0 % C::kSlots));
-                    if (it.nkv == 1) mma_commit(bar_q_empty);
-                }
+        const uint32_t t_s = tmem + s * BN;
+        const uint32_t t_o = tmem + 2 * BN + s * D;
+        const uint32_t t_p = C::kPAlias ? t_s : tmem + 2 * BN + 2 * D + s * (BN / 2);
+        const uint32_t bar_sf = bar_s_full + 8 * s, bar_pf = bar_p_full + 8 * s;
+        const uint32_t tok_me = kTokenBar + s, tok_other = kTokenBar + 1 - s;
+        // Turn protocol.  Every turn: this warp's (bounded) waits, then the
+        // token; a warp that must stop (a wait gave up, or the CTA aborts)
+        // raises the exit flag and still passes the token, so the other warp,
+        // which reads the flag right after taking the token, never waits on
+        // a token that will not come.
+        auto turn_begin = [&](bool waits_ok) -> bool {
+            named_bar_sync(tok_me, 64);
+            if (*exit_flag) return false;
+            if (!waits_ok || *abort_flag) {
+                *exit_flag = 1;
+                __threadfence_block();
                 __syncwarp();
-                for (int j = 0; j < it.nkv; ++j) {
-                    const uint32_t li_v = l0 + 2 * j + 1, li_kn = li_v + 1;
-                    // query tile s reads K/V tiles [a_s, nk_s); a tile that starts
-                    // at j + 1 has no softmax of tile j to wait for
-                    const bool need0 = j + 1 < it.nk0, need1 = j + 1 < it.nk1 && j + 1 >= (WIN ? it.a1 : 0);
-                    if (need0 || need1) {
-                        if (!ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8)) { ok = false; break; }
-                        const uint64_t dkn = dk_ring + (li_kn % C::kSlots) * kSlotDesc;
-                        if (need0) {
-                            if (!warp_wait(bar_s_free, fc0 & 1, wc, 10)) { ok = false; break; }
-                            ++fc0;
-                            tc_fence_after();
-                            if (elect_one()) {
-                                issue_qk<D>(t_s0, dq0, dkn);
-                                mma_commit(bar_s_full);
-                            }
-                            __syncwarp();
-                        }
-                        if (need1) {
-                            if (j >= (WIN ? it.a1 : 0)) {
-                                if (!warp_wait(bar_s_free + 8, fc1 & 1, wc, 11)) { ok = false; break; }
-                                ++fc1;
-                            }
-                            tc_fence_after();
-                            if (elect_one()) {
-                                issue_qk<D>(t_s1, dq1, dkn);
-                                mma_commit(bar_s_full + 8);
-                            }
-                            __syncwarp();
-                        }
-                        if (elect_one()) {  // K_{j+1} has had its last reader issued
-                            mma_commit(bar_kv_empty + 8 * (li_kn % C::kSlots));
-                            if (j + 1 == it.nkv - 1) mma_commit(bar_q_empty);
-                        }
-                        __syncwarp();
-                    }
-                    if (!ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5)) { ok = false; break; }
-                    const uint64_t dv = dv_ring + (li_v % C::kSlots) * kSlotDesc;
-                    if (j < it.nk0) {
-                        if (!warp_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
-                        ++pc0;
-                        tc_fence_after();
-                        if (elect_one()) {
-                            issue_pv<D>(t_o0, t_p0, dv, j > 0 ? 1u : 0u);
-                            mma_commit(bar_pv_done);
-                        }
-                        __syncwarp();
-                    }
-                    if (j < it.nk1 && j >= (WIN ? it.a1 : 0)) {
-                        if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
-                        ++pc1;
-                        tc_fence_after();
-                        if (elect_one()) {
-                            issue_pv<D>(t_o1, t_p1, dv, j > (WIN ? it.a1 : 0) ? 1u : 0u);
-                            mma_commit(bar_pv_done + 8);
-                        }
-                        __syncwarp();
-                    }
-                    if (elect_one()) mma_commit(bar_kv_empty + 8 * (li_v % C::kSlots));
-                    __syncwarp();
-                }
+                named_bar_arrive(tok_other, 64);
+                return false;
             }
-        }
-        for (int k = 0; C::kPAlias && ok && k * G < p.num_items; ++k) {
+            tc_fence_after();
+            return true;
+        };
+        auto turn_end = [&]() {
+            __syncwarp();
+            named_bar_arrive(tok_other, 64);
+        };
+        if (s == 1) named_bar_arrive(kTokenBar, 64);  // tile 0's warp takes the first turn
+        uint32_t lc = 0, items = 0, pc = 0, fc = 0;   // ring loads, items, P_full / S_free phases
+        bool run = true;
+        for (int k = 0; run && k * G < p.num_items; ++k) {
             const int idx = snake_item(k, cta, G);
             if (idx >= p.num_items) continue;
             Item it;
             if (!decode_item<OUT == kOutPart, WIN>(p, sched, idx, it)) continue;
-            if (!warp_wait(bar_q_full, items & 1, wc, 3)) { ok = false; break; }
+            // this tile reads K/V tiles [a_s, nk_s) of the item
+            const int a_s = s == 0 ? 0 : (WIN ? it.a1 : 0);
+            const int nk_s = s == 0 ? it.nk0 : it.nk1;
+            bool okw = warp_wait(bar_q_full, items & 1, wc, 3);
             ++items;
-            tc_fence_after();
-            // K_j and V_j are ring loads number lc + 2j and lc + 2j + 1.
+            // K_j and V_j are ring loads number l0 + 2j and l0 + 2j + 1.
             const uint32_t l0 = lc;
             lc += 2 * it.nkv;
             const uint32_t s_k0 = l0 % C::kSlots;
-            if (!warp_wait(bar_kv_full + 8 * s_k0, (l0 / C::kSlots) & 1, wc, 4)) { ok = false; break; }
-            tc_fence_after();
-            // prologue: S_s = Q_s K_0^T; K_0 is read only by these, release it.
+            // prologue: S_s = Q_s K_0^T when the tile starts at tile 0 (in
+            // split mode tile 0's range can be empty)
+            const bool first = nk_s > a_s && a_s == 0;
+            if (okw && first) okw = warp_wait(bar_kv_full + 8 * s_k0, (l0 / C::kSlots) & 1, wc, 4);
+            if (!turn_begin(okw)) {
+                run = false;
+                break;
+            }
             if (elect_one()) {
-                // Query tile 0's range starts at t0; in split mode it can be
-                // empty (the last key range of a short causal block).
-                if (it.nk0 > 0) {
-                    issue_qk<D>(t_s0, dq0, dk_ring + s_k0 * kSlotDesc);
-                    mma_commit(bar_s_full);
-                }
-                if (it.nk1 > 0 && (WIN ? it.a1 : 0) == 0) {
-                    issue_qk<D>(t_s1, dq1, dk_ring + s_k0 * kSlotDesc);
-                    mma_commit(bar_s_full + 8);
+                if (first) {
+                    issue_qk<D>(t_s, dq_s, dk_ring + s_k0 * kSlotDesc);
+                    mma_commit(bar_sf);
                 }
                 mma_commit(bar_kv_empty + 8 * s_k0);
                 if (it.nkv == 1) mma_commit(bar_q_empty);
             }
-            __syncwarp();
+            turn_end();
             for (int j = 0; j < it.nkv; ++j) {
                 const uint32_t li_v = l0 + 2 * j + 1, li_kn = li_v + 1;
                 const uint32_t s_v = li_v % C::kSlots, s_kn = li_kn % C::kSlots;
-                if (!warp_wait(bar_kv_full + 8 * s_v, (li_v / C::kSlots) & 1, wc, 5)) { ok = false; break; }
-                tc_fence_after();
                 const uint64_t dv = dv_ring + s_v * kSlotDesc;
                 const uint64_t dkn = dk_ring + s_kn * kSlotDesc;
-                bool kn_ready = false;
-                // query tile 0: O_0 (+)= P_0 V_j, then S_0 = Q_0 K_{j+1}^T
-                if (j < it.nk0) {
-                    if (!warp_wait(bar_p_full, pc0 & 1, wc, 6)) { ok = false; break; }
-                    ++pc0;
-                    const bool more = j + 1 < it.nk0;
-                    if (more) {
-                        if (!warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 8)) {
-                            ok = false;
-                            break;
-                        }
-                        kn_ready = true;
+                const bool reads = j >= a_s && j < nk_s;                   // P_s V_j
+                const bool next = j + 1 >= a_s && j + 1 < nk_s;            // Q_s K_{j+1}^T
+                if (C::kPAlias) {
+                    // D=128: one turn per tile: O_s (+)= P_s V_j, then
+                    // S_s = Q_s K_{j+1}^T (P_s overwrites S_s, so the next
+                    // Q K^T must follow P V); a tile whose range starts at
+                    // j + 1 issues its first Q K^T here.
+                    okw = true;
+                    if (reads) {
+                        okw = ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5) &&
+                              warp_wait(bar_pf, pc & 1, wc, 6 + s);
+                        ++pc;
                     }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_pv<D>(t_o0, t_s0, dv, j > 0 ? 1u : 0u);
-                        if (more) {
-                            issue_qk<D>(t_s0, dq0, dkn);
-                            mma_commit(bar_s_full);
-                        } else {
-                            mma_commit(bar_o_final);
-                        }
-                    }
-                    __syncwarp();
-                }
-                // query tile 1 (reads tiles [a1, nk1): with a left window bound it
-                // may start after tile 0)
-                if (j < it.nk1 && j >= (WIN ? it.a1 : 0)) {
-                    if (!warp_wait(bar_p_full + 8, pc1 & 1, wc, 7)) { ok = false; break; }
-                    ++pc1;
-                    const bool more = j + 1 < it.nk1;
-                    if (more && !kn_ready) {
-                        if (!warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 9)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_pv<D>(t_o1, t_s1, dv, j > (WIN ? it.a1 : 0) ? 1u : 0u);
-                        if (more) {
-                            issue_qk<D>(t_s1, dq1, dkn);
-                            mma_commit(bar_s_full + 8);
-                        } else {
-                            mma_commit(bar_o_final + 8);
-                        }
-                    }
-                    __syncwarp();
-                } else if (j + 1 == (WIN ? it.a1 : 0) && it.nk1 > (WIN ? it.a1 : 0)) {
-                    // query tile 1 starts at tile j + 1: its first Q K^T
-                    if (!kn_ready &&
-                        !warp_wait(bar_kv_full + 8 * s_kn, (li_kn / C::kSlots) & 1, wc, 9)) {
-                        ok = false;
+                    if (okw && next) okw = ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8 + s);
+                    if (!turn_begin(okw)) {
+                        run = false;
                         break;
                     }
-                    tc_fence_after();
                     if (elect_one()) {
-                        issue_qk<D>(t_s1, dq1, dkn);
-                        mma_commit(bar_s_full + 8);
+                        if (reads) issue_pv<D>(t_o, t_p, dv, j > a_s ? 1u : 0u);
+                        if (next) {
+                            issue_qk<D>(t_s, dq_s, dkn);
+                            mma_commit(bar_sf);
+                        } else if (reads) {
+                            mma_commit(bar_o_final + 8 * s);
+                        }
+                        // K_{j+1} and V_j: this warp's reads of them are issued
+                        if (j + 1 < it.nkv) mma_commit(bar_kv_empty + 8 * s_kn);
+                        if (j == it.nkv - 2) mma_commit(bar_q_empty);  // the item's last Q K^T
+                        mma_commit(bar_kv_empty + 8 * s_v);
                     }
-                    __syncwarp();
+                    turn_end();
+                } else {
+                    // D=64: P_s has its own TMEM columns.  Turn 1: the next
+                    // S_s as soon as the softmax has read S_s; turn 2: P_s V_j.
+                    if (j + 1 < it.nkv) {
+                        okw = true;
+                        if (next) {
+                            okw = ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8 + s);
+                            // a tile that starts at j + 1 has no softmax of tile j to wait for
+                            if (okw && j >= a_s) {
+                                okw = warp_wait(bar_s_free + 8 * s, fc & 1, wc, 10 + s);
+                                ++fc;
+                            }
+                        }
+                        if (!turn_begin(okw)) {
+                            run = false;
+                            break;
+                        }
+                        if (elect_one()) {
+                            if (next) {
+                                issue_qk<D>(t_s, dq_s, dkn);
+                                mma_commit(bar_sf);
+                            }
+                            mma_commit(bar_kv_empty + 8 * s_kn);  // K_{j+1} has had this warp's reader
+                            if (j + 1 == it.nkv - 1) mma_commit(bar_q_empty);
+                        }
+                        turn_end();
+                    }
+                    okw = true;
+                    if (reads) {
+                        okw = ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5) &&
+                              warp_wait(bar_pf, pc & 1, wc, 6 + s);
+                        ++pc;
+                    }
+                    if (!turn_begin(okw)) {
+                        run = false;
+                        break;
+                    }
+                    if (elect_one()) {
+                        if (reads) {
+                            issue_pv<D>(t_o, t_p, dv, j > a_s ? 1u : 0u);
+                            mma_commit(bar_pv_done + 8 * s);
+                        }
+                        mma_commit(bar_kv_empty + 8 * s_v);
+                    }
+                    turn_end();
                 }
-                // K_{j+1} has had its last reader (Q_s K_{j+1}^T) issued above and
-                // V_j its last (P_1 V_j): release both slots as soon as those
-                // MMAs complete.  Releasing K one tile ahead of V gives the
-                // producer an extra tile of lead on the next K load.
-                if (elect_one()) {
-                    if (j + 1 < it.nkv) mma_commit(bar_kv_empty + 8 * s_kn);
-                    if (j == it.nkv - 2) mma_commit(bar_q_empty);  // last Q K^T of the item issued
-                    mma_commit(bar_kv_empty + 8 * s_v);
-                }
-                __syncwarp();
             }
         }
         // Teardown: wait for every MMA issued so far before TMEM is freed.
@@ -890,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarpA) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
