@@ -51,7 +51,95 @@ struct BwdTcParams {
     int wl, wr;           // band: key j visible to row i iff i - wl <= j <= i + wr (< 0: unbounded)
     uint32_t *err;
     uint64_t wait_limit_ns;
+    int num_seqs;         // packed batch: sequences
+    int compact;          // packed batch: walk the compact order (bwd_decode_compact)
+    int head_group;       // compact order: number of near-equal head groups
 };
+
+// Packed batches with at most kMaxBwdSchedSeqs sequences and
+// kMaxBwdSchedLevels 128-row blocks per sequence walk a compact order: only
+// blocks that hold rows, heads in groups whose streamed operands (Q and dO
+// for dK/dV, K and V for dQ) stay in L2 while the group's items run.
+constexpr int kMaxBwdSchedSeqs = 255;
+constexpr int kMaxBwdSchedLevels = 128;
+constexpr int kBwdSchedBytes = 416;  // ranked[256] + reach[128] (bytes) + the item count
+#ifndef FA_BWD_GROUP_MB
+#define FA_BWD_GROUP_MB 96
+#endif
+constexpr double kBwdL2GroupBytes = FA_BWD_GROUP_MB * 1024.0 * 1024;
+
+// The compact order's table in shared memory: the sequences ranked by block
+// count (longest first, ties by index) and, per block level L, how many
+// sequences have more than L blocks.  Every CTA builds the same table.
+struct BwdSched {
+    const uint8_t *ranked;  // [num_seqs]
+    const uint8_t *reach;   // [nblk]
+    int per_head;           // blocks per head: the sum of reach over the levels
+};
+
+// Build the table at `tab` (all threads of the CTA; `scratch` holds an int
+// per sequence and is generic-proxy memory the TMA overwrites afterwards).
+__device__ __forceinline__ void build_bwd_sched(const BwdTcParams &p, uint8_t *tab, int *scratch) {
+    for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+        int64_t start;
+        int len;
+        seq_bounds(p.cu, q, p.total, p.n, p.err, start, len);  // invalid: len = 0
+        scratch[q] = (len + kT - 1) / kT;
+    }
+    __syncthreads();
+    uint8_t *ranked = tab, *reach = tab + 256;
+    for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+        const int nq = scratch[q];
+        int rank = 0;
+        for (int t = 0; t < p.num_seqs; ++t) rank += (scratch[t] > nq) || (scratch[t] == nq && t < q);
+        ranked[rank] = (uint8_t)q;
+    }
+    for (int L = threadIdx.x; L < p.nblk; L += blockDim.x) {
+        int r = 0;
+        for (int t = 0; t < p.num_seqs; ++t) r += scratch[t] > L;
+        reach[L] = (uint8_t)r;
+    }
+    if (threadIdx.x == 0) {
+        int total = 0;
+        for (int t = 0; t < p.num_seqs; ++t) total += scratch[t];
+        *reinterpret_cast<int *>(tab + 400) = total;
+    }
+    // the scratch's generic-proxy use is over before TMA (async proxy) writes it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ BwdSched bwd_sched(const BwdTcParams &p, const uint8_t *tab) {
+    return BwdSched{tab, tab + 256, p.compact ? *reinterpret_cast<const int *>(tab + 400) : 0};
+}
+
+// Item `idx` of the compact order: heads in p.head_group near-equal groups;
+// within a group block level L (from the first block up, or from the last
+// block down), then the sequences that reach L (longest first), then the
+// group's heads.
+__device__ __forceinline__ bool bwd_decode_compact(const BwdTcParams &p, const BwdSched &sc, int idx,
+                                                   bool from_top, int &unit, int &blk) {
+    // p.head_group near-equal groups: group g holds heads [g H / n, (g + 1) H / n)
+    const int ng = p.head_group;
+    int grp = 0, h0 = 0, hn = 0;
+    for (; grp < ng; ++grp) {
+        h0 = grp * p.heads / ng;
+        hn = (grp + 1) * p.heads / ng - h0;
+        if (idx < sc.per_head * hn) break;
+        idx -= sc.per_head * hn;
+    }
+    if (grp == ng) return false;
+    int L = from_top ? p.nblk - 1 : 0;
+    for (;;) {
+        if (L < 0 || L >= p.nblk) return false;
+        const int here = (int)sc.reach[L] * hn;
+        if (idx < here) break;
+        idx -= here;
+        L += from_top ? -1 : 1;
+    }
+    unit = (int)sc.ranked[idx / hn] * p.heads + h0 + idx % hn;
+    blk = L;
+    return true;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -152,7 +240,8 @@ struct DkCfg {
     static constexpr int kStatBytes = 2 * 2 * 64 * 4;   // [half parity][L, delta][64]
     static constexpr int kBarOff = kStatOff + kStatBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+    static constexpr int kSchedOff = kBarOff + kBarBytes;   // packed-batch walk table
+    static constexpr int kSmemBytes = kSchedOff + kBwdSchedBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(8 * (2 + 2 * kSlots + 7) + 16 <= kBarBytes, "barrier area");
 };
@@ -171,8 +260,23 @@ struct DkBars {
 // numbered key block first (lowest first: under the causal mask it has the
 // most query rows), then problem; CTA c takes items c, 2G-1-c, 2G+c, ...
 // Blocks past the end of their sequence are skipped.
-__device__ __forceinline__ bool next_dk_item(const BwdTcParams &p, int &k, int cta, int G, int D, Seq &sq,
-                                             int &j0) {
+__device__ __forceinline__ bool next_dk_item(const BwdTcParams &p, const BwdSched &sc, int &k, int cta, int G,
+                                             int D, Seq &sq, int &j0) {
+    if (p.compact) {  // key block from the first (most query rows under the causal mask) up
+        const int items = sc.per_head * p.heads;
+        for (; k * G < items; ++k) {
+            const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+            int unit, blk;
+            if (idx >= items || !bwd_decode_compact(p, sc, idx, false, unit, blk)) continue;
+            sq = seq_of(p, unit, D);
+            j0 = blk * kT;
+            if (j0 < sq.len) {
+                ++k;
+                return true;
+            }
+        }
+        return false;
+    }
     const int items = p.nblk * p.units;
     for (; k * G < items; ++k) {
         const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
@@ -262,9 +366,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // the packed-batch walk table (scratch: the not yet used ring)
+    uint8_t *sched_tab = gbase + C::kSchedOff;
+    if (p.compact) build_bwd_sched(p, sched_tab, reinterpret_cast<int *>(gbase + C::kRingOff));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const BwdSched sched = bwd_sched(p, sched_tab);
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
     const uint32_t ring = base + C::kRingOff;
@@ -276,7 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool ok = true;
             Seq sq;
             int j0;
-            while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+            while (ok && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
                 int i_first, halves;
                 dk_rows<WIN>(p, j0, sq.len, i_first, halves);
                 if (it > 0 && !mbar_wait(b.kv_free, (it - 1) & 1, wc, 0x40)) break;
@@ -313,7 +421,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         Seq sq;
         int j0;
-        while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+        while (ok && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
             int i_first, halves;
             dk_rows<WIN>(p, j0, sq.len, i_first, halves);
             if (!warp_wait(b.fix_full, it & 1, wc, 0x50)) break;
@@ -380,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         Seq sq;
         int j0;
-        while (ok && next_dk_item(p, k, cta, G, D, sq, j0)) {
+        while (ok && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
             const int n = sq.len;
             int i_first, halves;
             dk_rows<WIN>(p, j0, n, i_first, halves);
@@ -517,7 +625,8 @@ struct DqCfg {
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+    static constexpr int kSchedOff = kBarOff + kBarBytes;   // packed-batch walk table
+    static constexpr int kSmemBytes = kSchedOff + kBwdSchedBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(8 * (2 + 2 * kSlots + 7) + 16 <= kBarBytes, "barrier area");
     static_assert(3 * kT + D <= (int)kTmemCols, "TMEM columns");
@@ -525,8 +634,23 @@ struct DqCfg {
 
 // The CTA's next dQ work item: query block first (highest first: under the
 // causal mask it has the most keys), then problem; snake over CTAs.
-__device__ __forceinline__ bool next_dq_item(const BwdTcParams &p, int &k, int cta, int G, int D, Seq &sq,
-                                             int &ib) {
+__device__ __forceinline__ bool next_dq_item(const BwdTcParams &p, const BwdSched &sc, int &k, int cta, int G,
+                                             int D, Seq &sq, int &ib) {
+    if (p.compact) {  // query block from the last (most keys under the causal mask) down
+        const int items = sc.per_head * p.heads;
+        for (; k * G < items; ++k) {
+            const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+            int unit, blk;
+            if (idx >= items || !bwd_decode_compact(p, sc, idx, true, unit, blk)) continue;
+            sq = seq_of(p, unit, D);
+            ib = blk;
+            if (ib * kT < sq.len) {
+                ++k;
+                return true;
+            }
+        }
+        return false;
+    }
     const int items = p.nblk * p.units;
     for (; k * G < items; ++k) {
         const int idx = k * G + ((k & 1) ? (G - 1 - cta) : cta);
@@ -605,9 +729,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // the packed-batch walk table (scratch: the not yet used ring)
+    uint8_t *sched_tab = gbase + C::kSchedOff;
+    if (p.compact) build_bwd_sched(p, sched_tab, reinterpret_cast<int *>(gbase + C::kRingOff));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const BwdSched sched = bwd_sched(p, sched_tab);
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.err, abort_flag, p.wait_limit_ns};
     const uint32_t ring = base + C::kRingOff;
@@ -619,7 +747,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t li = 0;          // ring loads issued
             bool ok = true;
             Seq sq;
-            while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+            while (ok && next_dq_item(p, sched, k, cta, G, D, sq, ib)) {
                 int t_lo, tiles;
                 dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
                 if (it > 0 && !mbar_wait(qd_free, (it - 1) & 1, wc, 0x43)) break;
@@ -656,7 +784,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t lb = 0, gt = 0;      // ring loads and tiles of earlier items
         bool ok = true;
         Seq sq;
-        while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+        while (ok && next_dq_item(p, sched, k, cta, G, D, sq, ib)) {
             int t_lo, tiles;
             dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
             // K_j is ring load lb + 2j, V_j load lb + 2j + 1; tile t uses S buffer (gt + t) & 1
@@ -732,7 +860,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gt = 0;
         bool ok = true;
         Seq sq;
-        while (ok && next_dq_item(p, k, cta, G, D, sq, ib)) {
+        while (ok && next_dq_item(p, sched, k, cta, G, D, sq, ib)) {
             const int n = sq.len;
             int t_lo, tiles;
             dq_tiles<WIN>(p, ib, n, t_lo, tiles);
@@ -864,6 +992,17 @@ fa_status launch(const FaBwdProblem &p) {
     k.wr = p.wr;
     k.err = p.err;
     k.wait_limit_ns = p.wait_limit_ns;
+    // Packed batches of few sequences walk the compact order, heads in groups
+    // whose streamed operands (Q and dO, or K and V: the same size) fit
+    // kBwdL2GroupBytes.
+    k.num_seqs = p.varlen ? p.num_seqs : 0;
+    k.compact = p.varlen && p.num_seqs <= kMaxBwdSchedSeqs && k.nblk <= kMaxBwdSchedLevels;
+    {
+        const double per_head = (double)p.total * D * 2 * 2;
+        long long hg = per_head > 0 ? (long long)(kBwdL2GroupBytes / per_head) : p.heads;
+        hg = hg < 1 ? 1 : (hg > p.heads ? p.heads : hg);
+        k.head_group = (int)((p.heads + hg - 1) / hg);   // groups of at most hg heads, near-equal
+    }
     const long long grid = (long long)k.nblk * p.units_bh;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
     static FaCtxSet ready;  // contexts set up for this instantiation
