@@ -36,6 +36,11 @@ constexpr int kT = kTcRows;          // 128 rows / keys per tile
 constexpr int kBwdThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
+// dK/dV kernel: a second MMA issuer warp (see its MMA role)
+constexpr int kDkThreads = 224;
+constexpr int kDkMmaWarpA = 5;      // issuer of half-tile buffer 0; allocates TMEM
+constexpr int kDkMmaWarpB = 6;      // issuer of half-tile buffer 1
+constexpr uint32_t kDkToken = 2;    // named barriers 2, 3 (1 is the elementwise warps')
 constexpr uint32_t kTmemCols = 512;
 
 struct BwdTcParams {
@@ -319,7 +324,7 @@ __device__ __forceinline__ void issue_acc_half(uint32_t d_tmem, uint32_t a_tmem,
 }
 
 template <int D, typename Tout, bool WIN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdTcParams p) {
@@ -337,13 +342,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const DkBars b(base + C::kBarOff, C::kSlots);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
+    volatile int *exit_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 12);
     float *stat = reinterpret_cast<float *>(gbase + C::kStatOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x, G = gridDim.x;
 
     if (warp == kProdWarp && lane == 0) {
         mbar_init(b.fix_full, 1);
-        mbar_init(b.kv_free, 1);
+        mbar_init(b.kv_free, 2);       // one commit per issuer
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(b.ring_full + 8 * i, 1);
             mbar_init(b.ring_empty + 8 * i, 1);
@@ -352,17 +358,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b.s_full + 8 * x, 1);
             mbar_init(b.p_full + 8 * x, 4);
         }
-        mbar_init(b.o_final, 1);
+        mbar_init(b.o_final, 2);       // one commit per issuer
         mbar_init(b.acc_free, 4);
-        mbar_init(b.drain, 1);
+        mbar_init(b.drain, 2);
         fence_barrier_init();
         *abort_flag = 0;
+        *exit_flag = 0;
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
     }
-    if (warp == kMmaWarp) {
+    if (warp == kDkMmaWarpA) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -409,49 +416,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int v = g > C::kSlots ? g - C::kSlots : 0; v < g; ++v)
                 mbar_drain(b.ring_full + 8 * (v % C::kSlots), (v / C::kSlots) & 1, lim);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kDkMmaWarpA || warp == kDkMmaWarpB) {
         // --------------------------------------------------------- MMA
+        // Two issuer warps, one per half-tile buffer x (the halves u with
+        // u % 2 == x).  tcgen05.mma issue is effectively synchronous with
+        // execution, so an issuer's barrier waits are tensor idle time unless
+        // the other issuer is issuing meanwhile: the warps take turns through
+        // a token (named barriers kDkToken + x), each doing its waits while
+        // the other issues.  Per item the turns are the two prologue halves,
+        // then one per half (an even number in all).  K, V and the
+        // accumulators are shared: their release barriers count a commit per
+        // issuer.  A warp that must stop raises the exit flag and still passes
+        // the token.
         constexpr uint64_t kTileDesc = C::kTileBytes >> 4, kSlotDesc = C::kSlotBytes >> 4;
         constexpr uint64_t kHalfDesc = C::kHalfBytes >> 4;
+        const int X = warp - kDkMmaWarpA;
         const uint64_t d_k = smem_desc(base, 16, 1024), d_v = d_k + kTileDesc;
         const uint64_t d_ring_k = smem_desc(ring, 16, 1024);                 // K-major view
         const uint64_t d_ring_mn = smem_desc(ring, C::kHalfAtom, 1024);      // MN-major view
         const uint32_t t_dv = tmem + 2 * kT, t_dk = t_dv + D;
+        const uint32_t t_st = tmem + X * 2 * 64, t_dpt = t_st + 64;        // this issuer's buffer
+        const uint32_t tok_me = kDkToken + X, tok_other = kDkToken + 1 - X;
+        auto turn_begin = [&](bool waits_ok) -> bool {
+            named_bar_sync(tok_me, 64);
+            if (*exit_flag) return false;
+            if (!waits_ok || *abort_flag) {
+                *exit_flag = 1;
+                __threadfence_block();
+                __syncwarp();
+                named_bar_arrive(tok_other, 64);
+                return false;
+            }
+            tc_fence_after();
+            return true;
+        };
+        auto turn_end = [&]() {
+            __syncwarp();
+            named_bar_arrive(tok_other, 64);
+        };
+        if (X == 1) named_bar_arrive(kDkToken, 64);   // buffer 0's issuer takes the first turn
         int k = 0, it = 0, g = 0;
-        bool ok = true;
+        bool run = true;
         Seq sq;
         int j0;
-        while (ok && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
+        while (run && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
             int i_first, halves;
-            dk_rows<WIN>(p, j0, sq.len, i_first, halves);
-            if (!warp_wait(b.fix_full, it & 1, wc, 0x50)) break;
-            // S^T_x, dP^T_x of the item's first two halves (buffer x = half & 1)
-            for (int u = 0; u < 2 && u < halves; ++u) {
-                if (!ring_wait(b.ring_full, g + u, C::kSlots, wc, 0x51)) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
-                    const uint64_t sl = ((g + u) % C::kSlots) * kSlotDesc;
-                    const uint32_t t_st = tmem + u * 2 * 64;
-                    issue_st_half<D>(t_st, d_k, d_ring_k + sl);
-                    issue_st_half<D>(t_st + 64, d_v, d_ring_k + sl + kHalfDesc);
-                    mma_commit(b.s_full + 8 * u);
-                }
-                __syncwarp();
+            dk_rows<WIN>(p, j0, sq.len, i_first, halves);   // halves is even
+            // prologue turn: S^T_X, dP^T_X of the item's half X
+            bool okw = warp_wait(b.fix_full, it & 1, wc, 0x50) &&
+                       ring_wait(b.ring_full, g + X, C::kSlots, wc, 0x51);
+            if (!turn_begin(okw)) break;
+            if (elect_one()) {
+                const uint64_t sl = ((g + X) % C::kSlots) * kSlotDesc;
+                issue_st_half<D>(t_st, d_k, d_ring_k + sl);
+                issue_st_half<D>(t_dpt, d_v, d_ring_k + sl + kHalfDesc);
+                mma_commit(b.s_full + 8 * X);
+                if (halves <= 2) mma_commit(b.kv_free);   // this issuer's last reader of K, V
             }
-            if (!ok) break;
-            if (halves <= 2) {                          // K and V have had their last reader
-                if (elect_one()) mma_commit(b.kv_free);
-                __syncwarp();
-            }
-            // the previous item's dK, dV have been read out of TMEM
-            if (it > 0 && !warp_wait(b.acc_free, (it - 1) & 1, wc, 0x59)) break;
+            turn_end();
             for (int u = 0; u < halves; ++u) {
-                const int gu = g + u, x = u & 1;
-                const uint32_t t_st = tmem + x * 2 * 64, t_dpt = t_st + 64;
-                if (!warp_wait(b.p_full + 8 * x, (gu >> 1) & 1, wc, 0x52)) { ok = false; break; }
+                if ((u & 1) != X) continue;   // the other issuer's half (its turn)
+                const int gu = g + u;
                 const bool next = u + 2 < halves;
-                if (next && !ring_wait(b.ring_full, gu + 2, C::kSlots, wc, 0x53)) { ok = false; break; }
-                tc_fence_after();
+                okw = warp_wait(b.p_full + 8 * X, (gu >> 1) & 1, wc, 0x52);
+                if (okw && next) okw = ring_wait(b.ring_full, gu + 2, C::kSlots, wc, 0x53);
+                // the previous item's dK, dV have been read out of TMEM (the
+                // first accumulating MMA of an item is half 0's)
+                if (okw && u == 0 && it > 0) okw = warp_wait(b.acc_free, (it - 1) & 1, wc, 0x59);
+                if (!turn_begin(okw)) {
+                    run = false;
+                    break;
+                }
                 if (elect_one()) {
                     const uint64_t sl = (gu % C::kSlots) * kSlotDesc;
                     const uint32_t acc = u > 0 ? 1u : 0u;
@@ -462,15 +497,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const uint64_t sn = ((gu + 2) % C::kSlots) * kSlotDesc;
                         issue_st_half<D>(t_st, d_k, d_ring_k + sn);
                         issue_st_half<D>(t_dpt, d_v, d_ring_k + sn + kHalfDesc);
-                        mma_commit(b.s_full + 8 * x);
-                        if (u + 2 == halves - 1) mma_commit(b.kv_free);   // last reader of K, V
+                        mma_commit(b.s_full + 8 * X);
+                        if (u + 4 >= halves) mma_commit(b.kv_free);   // this issuer's last reader of K, V
+                    } else {
+                        mma_commit(b.o_final);   // this issuer's last accumulation of the item
                     }
                 }
-                __syncwarp();
+                turn_end();
             }
-            if (!ok) break;
-            if (elect_one()) mma_commit(b.o_final);
-            __syncwarp();
             g += halves;
             ++it;
         }
@@ -598,7 +632,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kDkMmaWarpA) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -948,11 +982,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <typename K>
-fa_status prepare(K kernel, int smem) {
+fa_status prepare(K kernel, int smem, int threads) {
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, kernel);
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    if (a.maxThreadsPerBlock < kBwdThreads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
+    if (a.maxThreadsPerBlock < threads) return fa_cuda_fail(cudaErrorLaunchOutOfResources);
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
@@ -1007,14 +1041,14 @@ fa_status launch(const FaBwdProblem &p) {
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
     static FaCtxSet ready;  // contexts set up for this instantiation
     const fa_status su = fa_once_per_context(ready, []() -> fa_status {
-        const fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes);
-        return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes) : st;
+        const fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes, kDkThreads);
+        return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes, kBwdThreads) : st;
     });
     if (su != FA_OK) return su;
     int grid_dk = p.grid_ctas > 0 ? p.grid_ctas : num_sms();   // persistent: one CTA per SM
     if (grid_dk <= 0) return FA_ERR_CUDA;
     if (grid_dk > grid) grid_dk = (int)grid;
-    bwd_dkdv_tc_kernel<D, Tout, WIN><<<grid_dk, kBwdThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv, tdo64,
+    bwd_dkdv_tc_kernel<D, Tout, WIN><<<grid_dk, kDkThreads, DkCfg<D>::kSmemBytes, p.stream>>>(tq64, tk, tv, tdo64,
                                                                                          k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
