@@ -20,8 +20,10 @@
 // operand).  The streamed operands (Q_i and dO_i, or K_j and V_j) flow
 // through a TMA ring.  Warps 0-3 turn S, dP into P, dS (one TMEM
 // lane, i.e. one key or one query row, per thread), warp 4 is the TMA
-// producer, warp 5 allocates TMEM and issues the MMAs.  Every wait is
-// bounded (the device watchdog of the forward kernel).
+// producer, warp 5 allocates TMEM.  In the dK/dV kernel warps 5 and 6
+// issue the MMAs in turns, one per half-tile buffer; in the dQ kernel warp 5
+// issues them alone.  Every wait is bounded (the device watchdog of the
+// forward kernel).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
