@@ -565,13 +565,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // S_s = Q_s K_{j+1}^T (P_s overwrites S_s, so the next
                     // Q K^T must follow P V); a tile whose range starts at
                     // j + 1 issues its first Q K^T here.
+                    // The ring loads are normally in place long before the
+                    // softmax hands over P_s: wait for them first, so that
+                    // only the token stands between P_full and the issue.
                     okw = true;
+                    if (reads) okw = ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5);
+                    if (okw && next) okw = ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8 + s);
                     if (reads) {
-                        okw = ring_wait(bar_kv_full, li_v, C::kSlots, wc, 5) &&
-                              warp_wait(bar_pf, pc & 1, wc, 6 + s);
+                        okw = okw && warp_wait(bar_pf, pc & 1, wc, 6 + s);
                         ++pc;
                     }
-                    if (okw && next) okw = ring_wait(bar_kv_full, li_kn, C::kSlots, wc, 8 + s);
                     if (!turn_begin(okw)) {
                         run = false;
                         break;
