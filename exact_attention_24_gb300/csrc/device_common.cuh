@@ -252,6 +252,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *r) {
         : "r"(taddr));
 }
 
+// Same load, and also the maximum of the 32 values each thread receives
+// (tcgen05.ld.red, sm_103a): the row maximum of a score tile comes with its
+// load instead of costing a reduction in registers.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, float *r, float &mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+          "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]),
+          "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]),
+          "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]),
+          "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]),
+          "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]), "=f"(mx)
+        : "r"(taddr));
+}
+
 // 32 lanes x 32 bit, 16 consecutive columns (store).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
     asm volatile(

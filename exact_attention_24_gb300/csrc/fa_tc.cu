@@ -685,23 +685,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(bar_s_full + 8 * s, sc & 1, wc, 16 + s)) { ok = false; break; }
                 ++sc;
                 tc_fence_after();
-                float x[BN];
-#pragma unroll
-                for (int cc = 0; cc < BN / 32; ++cc)
-                    tmem_ld32(t_s + cc * 32, x + cc * 32);
-                tmem_wait_ld();
-                if (!C::kPAlias && j + 1 < nks) {
-                    // S_s is in registers: the MMA warp may compute the next S_s.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_s_free + 8 * s);
-                }
                 const int key0 = key_base + j * BN;
                 // Rows of this query tile are row - r .. row - r + 127; a tile needs
                 // masking if it crosses the sequence end or a window edge.
                 const bool need_mask = (key0 + BN > len) ||
                                        (p.wr >= 0 && key0 + BN - 1 > row - r + p.wr) ||
                                        (win_l >= 0 && key0 < row - r + 127 - win_l);
+                float x[BN];
+                float mx;
+                if (!need_mask) {
+                    // the row maximum comes with the load
+                    float m4[BN / 32];
+#pragma unroll
+                    for (int cc = 0; cc < BN / 32; ++cc)
+                        tmem_ld32_max(t_s + cc * 32, x + cc * 32, m4[cc]);
+                    tmem_wait_ld();
+                    mx = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < BN / 32; ++cc)
+                        tmem_ld32(t_s + cc * 32, x + cc * 32);
+                    tmem_wait_ld();
+                }
+                if (!C::kPAlias && j + 1 < nks) {
+                    // S_s is in registers: the MMA warp may compute the next S_s.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_s_free + 8 * s);
+                }
                 if (need_mask) {
                     // keys in [lo_lim, hi_lim) are live for this row
                     const int hi_lim = p.wr >= 0 ? min(row + p.wr + 1, len) : len;
@@ -709,17 +720,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
                         if (key0 + i >= hi_lim || key0 + i < lo_lim) x[i] = -INFINITY;
+                    // Row max of the masked scores: 8 independent chains of
+                    // 3-input max, then a tree.
+                    float mx8[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(x[k], x[8 + k]);
+#pragma unroll
+                    for (int t = 2; t < 16; t += 2)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], x[8 * t + k], x[8 * t + 8 + k]);
+                    mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                               max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 }
-                // Row max: 8 independent chains of 3-input max, then a tree.
-                float mx8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(x[k], x[8 + k]);
-#pragma unroll
-                for (int t = 2; t < 16; t += 2)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], x[8 * t + k], x[8 * t + 8 + k]);
-                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_use, mx);
                 const bool move = (m_new - m_use) * c > kRescaleThreshold;
                 float alpha = 1.f;
