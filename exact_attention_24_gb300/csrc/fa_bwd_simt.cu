@@ -111,6 +111,46 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const T *o, const T *dou
     if (lane == 0) delta[heads > 0 ? (row % heads) * total + row / heads : row] = s;
 }
 
+// Same, with 16-byte loads: V = D * sizeof(T) / 16 threads per row (8, 16
+// or 32), each taking one 16-byte piece of O and of dO, then a sum over the
+// row's V lanes.  Needs O and dO 16-byte aligned (D is 64 or 128).
+__device__ __forceinline__ float dot16(const uint4 &a, const uint4 &b, float) {
+    const float *x = reinterpret_cast<const float *>(&a), *y = reinterpret_cast<const float *>(&b);
+    return fmaf(x[0], y[0], fmaf(x[1], y[1], fmaf(x[2], y[2], x[3] * y[3])));
+}
+__device__ __forceinline__ float dot16(const uint4 &a, const uint4 &b, __nv_bfloat16) {
+    const __nv_bfloat162 *x = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    const __nv_bfloat162 *y = reinterpret_cast<const __nv_bfloat162 *>(&b);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 u = __bfloat1622float2(x[i]), v = __bfloat1622float2(y[i]);
+        s = fmaf(u.x, v.x, fmaf(u.y, v.y, s));
+    }
+    return s;
+}
+template <typename T, int V>
+__global__ void __launch_bounds__(256) bwd_delta16_kernel(const T *o, const T *dout, float *delta,
+                                                          int64_t rows, int heads, int64_t total) {
+    // Launched with programmatic stream serialization.  The next kernel is
+    // released only as the CTAs finish: released at the start, its CTAs
+    // would take registers from this memory-bound kernel's later CTAs.
+    pdl_wait();
+    const int64_t row = ((int64_t)blockIdx.x * 256 + threadIdx.x) / V;
+    const int part = threadIdx.x % V;
+    const bool live = row < rows;
+    float s = 0.f;
+    if (live) {
+        const uint4 a = reinterpret_cast<const uint4 *>(o)[row * V + part];
+        const uint4 b = reinterpret_cast<const uint4 *>(dout)[row * V + part];
+        s = dot16(a, b, T());
+    }
+#pragma unroll
+    for (int off = V / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (live && part == 0) delta[heads > 0 ? (row % heads) * total + row / heads : row] = s;
+    pdl_launch_dependents();
+}
+
 // Rows [r0, r0 + kTile) of a head (row stride rs elements) into shared
 // memory as float32 (zero past n).
 template <int D, typename T>
@@ -354,6 +394,9 @@ fa_status fa_launch_bwd_delta(const FaBwdProblem &p) {
     if (rows == 0) return FA_OK;
     const int64_t grid = (rows + 7) / 8;
     if (grid > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    // 16-byte pieces per row: 8, 16 or 32 threads per row
+    const int vec = p.D * (p.dtype == FA_F32 ? 4 : 2) / 16;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(p.o) | reinterpret_cast<uintptr_t>(p.dout)) & 15u) == 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(256);
@@ -364,7 +407,27 @@ fa_status fa_launch_bwd_delta(const FaBwdProblem &p) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (p.dtype == FA_F32)
+    if (aligned && (vec == 8 || vec == 16 || vec == 32)) {
+        const int64_t g16 = (rows * vec + 255) / 256;
+        if (g16 > INT32_MAX) return FA_ERR_UNSUPPORTED;
+        cfg.gridDim = dim3((unsigned)g16);
+        const float *of = static_cast<const float *>(p.o), *df = static_cast<const float *>(p.dout);
+        const __nv_bfloat16 *ob = static_cast<const __nv_bfloat16 *>(p.o);
+        const __nv_bfloat16 *db = static_cast<const __nv_bfloat16 *>(p.dout);
+        const bool f32 = p.dtype == FA_F32;
+        if (vec == 8)
+            e = f32 ? cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<float, 8>, of, df, p.delta, rows, heads, p.total)
+                    : cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<__nv_bfloat16, 8>, ob, db, p.delta, rows,
+                                         heads, p.total);
+        else if (vec == 16)
+            e = f32 ? cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<float, 16>, of, df, p.delta, rows, heads, p.total)
+                    : cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<__nv_bfloat16, 16>, ob, db, p.delta, rows,
+                                         heads, p.total);
+        else
+            e = f32 ? cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<float, 32>, of, df, p.delta, rows, heads, p.total)
+                    : cudaLaunchKernelEx(&cfg, fa::bwd_delta16_kernel<__nv_bfloat16, 32>, ob, db, p.delta, rows,
+                                         heads, p.total);
+    } else if (p.dtype == FA_F32)
         e = cudaLaunchKernelEx(&cfg, fa::bwd_delta_kernel<float>, static_cast<const float *>(p.o),
                                static_cast<const float *>(p.dout), p.delta, rows, p.D, heads, p.total);
     else
