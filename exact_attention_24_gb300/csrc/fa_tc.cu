@@ -695,12 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mx;
                 if (!need_mask) {
                     // the row maximum comes with the load
-                    float m4[BN / 32];
-#pragma unroll
-                    for (int cc = 0; cc < BN / 32; ++cc)
-                        tmem_ld32_max(t_s + cc * 32, x + cc * 32, m4[cc]);
+                    tmem_ld128_max(t_s, x, mx);
                     tmem_wait_ld();
-                    mx = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
                 } else {
 #pragma unroll
                     for (int cc = 0; cc < BN / 32; ++cc)
