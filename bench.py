@@ -1156,9 +1156,9 @@ def main(argv=None):
     else:
         w = WORKLOADS[args.workload]
     if args.record_traffic:
-        e = record_traffic(args.record_traffic, "fa_bwd" if args.bwd else "fa_tc", w.name,
-                           args.captured_with)
-        print(json.dumps({f"{'fa_bwd' if args.bwd else 'fa_tc'}/{w.name}": e}), flush=True)
+        tag = "fa_bwd" if args.bwd else ("fa_simt" if w.dtype == "f32" else "fa_tc")
+        e = record_traffic(args.record_traffic, tag, w.name, args.captured_with)
+        print(json.dumps({f"{tag}/{w.name}": e}), flush=True)
         return 0
     rank, world, local = dist_env()
     if world != args.gpus:
