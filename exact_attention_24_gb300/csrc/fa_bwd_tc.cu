@@ -658,6 +658,9 @@ template <int D>
 struct DqCfg {
     static constexpr int kTileBytes = kT * D * 2;
     static constexpr int kSlots = D == 128 ? 5 : 10;
+    // D = 128: K_t is loaded twice, for S_t and for dQ_t, rather than held
+    // from one to the other (see the producer).  D = 64 has slots to spare.
+    static constexpr bool kReloadK = D == 128;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     static constexpr int kBarBytes = 256;
@@ -791,17 +794,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 load_rows<D>(base, &tm_q, fix_full, ib * kT, sq, p.varlen, kTcAtomBytes);
                 load_rows<D>(base + C::kTileBytes, &tm_do, fix_full, ib * kT, sq, p.varlen, kTcAtomBytes);
                 ++it;
-                for (int j = 0; ok && j < tiles; ++j) {
-                    for (int kv = 0; kv < 2; ++kv, ++li) {
-                        const uint32_t slot = li % C::kSlots, round = li / C::kSlots;
-                        if (round > 0 && !mbar_wait(kv_empty + 8 * slot, (round - 1) & 1, wc, 0x42)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
-                        load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
-                                     (t_lo + j) * kT, sq, p.varlen, kTcAtomBytes);
-                    }
+                // kReloadK: one reader per ring load, in the order the MMA warp
+                // reads them: K_0 (S_0), V_0 (dP_0), K_1 (S_1), then per tile t:
+                // V_{t+1} (dP_{t+1}), K_t again (dQ_t), K_{t+2} (S_{t+2}).  Held
+                // from S_t to dQ_t instead, three K tiles and a V tile fill four of
+                // the five 32 KB slots at D = 128, and the next loads wait for
+                // slots.  Otherwise K_j, V_j in turn, K_j read by S_j and dQ_j.
+                auto load = [&](int kv, int j) -> bool {
+                    const uint32_t slot = li % C::kSlots, round = li / C::kSlots;
+                    if (round > 0 && !mbar_wait(kv_empty + 8 * slot, (round - 1) & 1, wc, 0x42)) return false;
+                    mbar_arrive_expect_tx(kv_full + 8 * slot, C::kTileBytes);
+                    load_rows<D>(ring + slot * C::kTileBytes, kv == 0 ? &tm_k : &tm_v, kv_full + 8 * slot,
+                                 (t_lo + j) * kT, sq, p.varlen, kTcAtomBytes);
+                    ++li;
+                    return true;
+                };
+                if (C::kReloadK) {
+                    ok = load(0, 0) && load(1, 0) && (tiles < 2 || load(0, 1));
+                    for (int t = 0; ok && t < tiles; ++t)
+                        ok = (t + 1 >= tiles || load(1, t + 1)) && load(0, t) && (t + 2 >= tiles || load(0, t + 2));
+                } else {
+                    for (int j = 0; ok && j < tiles; ++j) ok = load(0, j) && load(1, j);
                 }
             }
             const uint64_t lim = p.wait_limit_ns;
@@ -823,35 +836,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         while (ok && next_dq_item(p, sched, k, cta, G, D, sq, ib)) {
             int t_lo, tiles;
             dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
-            // K_j is ring load lb + 2j, V_j load lb + 2j + 1; tile t uses S buffer (gt + t) & 1
-            if (!warp_wait(fix_full, it & 1, wc, 0x54) || !ring_wait(kv_full, lb, C::kSlots, wc, 0x55) ||
-                !ring_wait(kv_full, lb + 1, C::kSlots, wc, 0x55))
+            // Ring loads in the producer's order: K_0 = lb, V_0 = lb + 1,
+            // K_1 = lb + 2 either way; then per tile t: V_{t+1}, K_t, K_{t+2}
+            // (kReloadK, one reader each), or K_j = lb + 2j, V_j = lb + 2j + 1.
+            // Tile t uses S buffer (gt + t) & 1.
+            uint32_t cur = lb;
+            const uint32_t ls0 = cur++, lv0 = cur++;
+            if (!warp_wait(fix_full, it & 1, wc, 0x54) || !ring_wait(kv_full, ls0, C::kSlots, wc, 0x55) ||
+                !ring_wait(kv_full, lv0, C::kSlots, wc, 0x55))
                 break;
             tc_fence_after();
             if (elect_one()) {
-                issue_qk<D>(tmem + (gt & 1) * kT, d_q, d_ring_k + (lb % C::kSlots) * kTileDesc);   // S_0
+                issue_qk<D>(tmem + (gt & 1) * kT, d_q, d_ring_k + (ls0 % C::kSlots) * kTileDesc);  // S_0
                 mma_commit(s_full + 8 * (gt & 1));
-                issue_qk<D>(t_dp, d_do, d_ring_k + ((lb + 1) % C::kSlots) * kTileDesc);            // dP_0
+                if (C::kReloadK) mma_commit(kv_empty + 8 * (ls0 % C::kSlots));
+                issue_qk<D>(t_dp, d_do, d_ring_k + (lv0 % C::kSlots) * kTileDesc);                 // dP_0
                 mma_commit(dp_full);
-                mma_commit(kv_empty + 8 * ((lb + 1) % C::kSlots));                                // V_0 read
+                mma_commit(kv_empty + 8 * (lv0 % C::kSlots));                                    // V_0 read
                 if (tiles == 1) mma_commit(qd_free);                                            // Q, dO read
             }
             __syncwarp();
             if (tiles > 1) {
-                if (!ring_wait(kv_full, lb + 2, C::kSlots, wc, 0x55)) break;
+                const uint32_t ls1 = cur++;
+                if (!ring_wait(kv_full, ls1, C::kSlots, wc, 0x55)) break;
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + ((lb + 2) % C::kSlots) * kTileDesc);
+                    issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + (ls1 % C::kSlots) * kTileDesc);
                     mma_commit(s_full + 8 * ((gt + 1) & 1));                                    // S_1
+                    if (C::kReloadK) mma_commit(kv_empty + 8 * (ls1 % C::kSlots));
                 }
                 __syncwarp();
             }
             for (int t = 0; t < tiles; ++t) {
                 const uint32_t g = gt + t;
                 const uint32_t t_buf = tmem + (g & 1) * kT;
-                if (!warp_wait(ds_full, g & 1, wc, 0x56)) { ok = false; break; }
-                const uint32_t lk = lb + 2 * t, lvn = lk + 3, lk2 = lk + 4;
+                uint32_t lvn, lk, lk2;   // V_{t+1}, K_t (for dQ_t), K_{t+2}
+                if (C::kReloadK) {
+                    lvn = t + 1 < tiles ? cur++ : 0u;
+                    lk = cur++;
+                    lk2 = t + 2 < tiles ? cur++ : 0u;
+                } else {
+                    lk = lb + 2 * t;
+                    lvn = lk + 3;
+                    lk2 = lk + 4;
+                }
+                // The loads first (they do not depend on the dS step), then dS_t;
+                // then one issue block: dP_{t+1}, dQ_t, S_{t+2}.
                 if (t + 1 < tiles && !ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) { ok = false; break; }
+                if (!ring_wait(kv_full, lk, C::kSlots, wc, 0x57)) { ok = false; break; }
+                if (t + 2 < tiles && !ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) { ok = false; break; }
+                if (!warp_wait(ds_full, g & 1, wc, 0x56)) { ok = false; break; }
                 // the previous item's dQ has been read out of TMEM
                 if (t == 0 && it > 0 && !warp_wait(acc_free, (it - 1) & 1, wc, 0x5a)) { ok = false; break; }
                 tc_fence_after();
@@ -864,22 +898,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     issue_pv<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
                     mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
-                }
-                __syncwarp();
-                if (t + 2 < tiles) {
-                    if (!ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) { ok = false; break; }
-                    tc_fence_after();
-                    if (elect_one()) {
+                    if (t + 2 < tiles) {
+                        // S_{t+2} overwrites dS_t's buffer after dQ_t has read it (in order)
                         issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
                         mma_commit(s_full + 8 * (g & 1));
+                        if (C::kReloadK) mma_commit(kv_empty + 8 * (lk2 % C::kSlots));
                     }
-                    __syncwarp();
                 }
+                __syncwarp();
             }
             if (!ok) break;
             if (elect_one()) mma_commit(o_final);
             __syncwarp();
-            lb += 2 * tiles;
+            lb = C::kReloadK ? cur : lb + 2 * tiles;
             gt += tiles;
             ++it;
         }
