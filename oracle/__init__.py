@@ -45,6 +45,7 @@ from .attention import (  # noqa: F401
     merge_partials,
 )
 from .backward import (  # noqa: F401
+    attention_bwd_magnitudes,
     attention_bwd_recompute,
     attention_bwd_ref,
     attention_bwd_ref_varlen,

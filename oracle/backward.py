@@ -99,6 +99,51 @@ def attention_bwd_ref(q, k, v, do, scale: float, causal: bool, window=None):
             delta.reshape(*lead, n))
 
 
+def attention_bwd_magnitudes(q, k, v, do, scale: float, causal: bool, window=None):
+    """Per-element magnitudes of the gradient sums, for error bounds.
+
+    Each gradient element is a sum of products (the five contractions of
+    "Application in Backward Pass (5 MMAs)"); rounding a factor of every
+    term by a relative u moves the sum by at most u times the sum of the
+    terms' absolute values.  These are those sums, from the same P and dP as
+    ``_bwd_head``, with every factor replaced by its absolute value, D_i
+    included (a sum itself, D_i = sum_c dO[i,c] O[i,c]):
+
+        M_dV = P^T |dO|,   |D|_i = sum_c |dO[i,c]| |O[i,c]|,
+        M_dS = P (|dP| + |D|_i),
+        M_dQ = scale M_dS |K|,   M_dK = scale M_dS^T |Q|.
+
+    By the triangle inequality |dQ| <= M_dQ, |dK| <= M_dK, |dV| <= M_dV
+    elementwise.  Same shapes and leading dimensions as attention_bwd_ref.
+    """
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    lead = qf.shape[:-2]
+    n, d = qf.shape[-2:]
+    dvd = vf.shape[-1]
+    nb = int(np.prod(lead, dtype=np.int64))
+    qf, kf = qf.reshape(nb, n, d), kf.reshape(nb, n, d)
+    vf, dof = vf.reshape(nb, n, dvd), dof.reshape(nb, n, dvd)
+    mq, mk, mv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    for h in range(nb):
+        if n == 0:
+            continue
+        keep = _mask(n, np.arange(n), causal, window)
+        s = np.where(keep, scale * (qf[h] @ kf[h].T), -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        live = np.isfinite(m[:, 0])
+        e = np.where(keep, np.exp(s - np.where(live[:, None], m, 0.0)), 0.0)
+        l = e.sum(axis=1, keepdims=True)
+        p = np.where(live[:, None], e / np.where(live[:, None], l, 1.0), 0.0)
+        o = p @ vf[h]
+        dp = dof[h] @ vf[h].T
+        dabs = np.sum(np.abs(dof[h]) * np.abs(o), axis=1)
+        mds = p * (np.abs(dp) + dabs[:, None])
+        mv[h] = p.T @ np.abs(dof[h])
+        mq[h] = scale * (mds @ np.abs(kf[h]))
+        mk[h] = scale * (mds.T @ np.abs(qf[h]))
+    return mq.reshape(*lead, n, d), mk.reshape(*lead, n, d), mv.reshape(*lead, n, dvd)
+
+
 def attention_bwd_ref_varlen(q, k, v, do, cu_seqlens, scale: float, causal: bool):
     """Varlen gradients: ``[total, H, D]`` packing, sequence s owns tokens
     ``cu[s] .. cu[s+1]-1`` and attends only within itself.  Returns

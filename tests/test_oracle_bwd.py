@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import (attention_bwd_recompute, attention_bwd_ref, attention_bwd_ref_varlen,
+from oracle import (attention_bwd_magnitudes, attention_bwd_recompute, attention_bwd_ref,
+                    attention_bwd_ref_varlen,
                     attention_ref, forward_for_backward)
 
 
@@ -278,3 +279,53 @@ def test_bwd_sampled_band_matches_definition():
         assert np.max(np.abs(dq - ref[0][rows])) <= 1e-13
         assert np.max(np.abs(dk - ref[1][keys])) <= 1e-13
         assert np.max(np.abs(dv - ref[2][keys])) <= 1e-13
+
+
+# ------------------------------------------------ gradient magnitudes --
+# attention_bwd_magnitudes gives, per gradient element, the sum of the
+# absolute values of its terms: the scale of the per-element error bound in
+# the GPU parity tests.  Pinned by the triangle inequality, by the case
+# without cancellation (equality) and by a one-key closed form.
+
+@pytest.mark.parametrize("causal, window", [(False, None), (True, None), (False, (5, 3))])
+def test_bwd_magnitudes_bound_the_gradients(causal, window):
+    rng = np.random.default_rng(11)
+    q, k, v, do = (rng.standard_normal((2, 41, 16)) for _ in range(4))
+    grads = attention_bwd_ref(q, k, v, do, 0.3, causal, window=window)[:3]
+    mags = attention_bwd_magnitudes(q, k, v, do, 0.3, causal, window=window)
+    for g, m in zip(grads, mags):
+        assert g.shape == m.shape
+        assert np.all(m >= 0)
+        assert np.all(np.abs(g) <= m * (1 + 1e-12) + 1e-300)
+        # a real bound, not a loose constant: somewhere within a factor 2
+        assert np.max(np.abs(g) / np.maximum(m, 1e-300)) > 0.5
+
+
+def test_bwd_magnitudes_equal_dv_without_cancellation():
+    rng = np.random.default_rng(12)
+    q, k, v = (rng.standard_normal((30, 8)) for _ in range(3))
+    do = np.abs(rng.standard_normal((30, 8)))          # P >= 0, dO >= 0: no cancellation in dV
+    dv = attention_bwd_ref(q, k, v, do, 0.5, True)[2]
+    mv = attention_bwd_magnitudes(q, k, v, do, 0.5, True)[2]
+    np.testing.assert_allclose(mv, dv, rtol=1e-13, atol=0)
+
+
+def test_bwd_magnitudes_one_key_closed_form():
+    """n = 1: P = 1, O = V, dP = dO.V = D, so dS = 0 and the gradients of Q, K
+    vanish, while their magnitudes are scale (|dO.V| + sum |dO| |V|) |K| (and
+    |Q|); M_dV = |dO|."""
+    q = np.array([[0.5, -2.0, 1.0, 3.0]])
+    k = np.array([[-1.0, 0.25, 2.0, -0.5]])
+    v = np.array([[1.0, 1.0, -2.0, 0.5]])
+    do = np.array([[1.0, -1.0, 0.5, 2.0]])
+    scale = 0.7
+    dq, dk, dv, _ = attention_bwd_ref(q, k, v, do, scale, False)
+    mq, mk, mv = attention_bwd_magnitudes(q, k, v, do, scale, False)
+    dpv = float((do @ v.T)[0, 0])                     # dO . V = D
+    dabs = float(np.sum(np.abs(do) * np.abs(v)))
+    np.testing.assert_allclose(dq, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-15)
+    np.testing.assert_allclose(mq, scale * (abs(dpv) + dabs) * np.abs(k), rtol=1e-15)
+    np.testing.assert_allclose(mk, scale * (abs(dpv) + dabs) * np.abs(q), rtol=1e-15)
+    np.testing.assert_allclose(mv, np.abs(do), rtol=1e-15)
+    np.testing.assert_allclose(dv, do, rtol=1e-15)
