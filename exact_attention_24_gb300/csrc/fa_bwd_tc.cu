@@ -18,12 +18,13 @@
 // Both are made of the forward pass's two MMA shapes (A B^T with both
 // operands K-major in shared memory; A from TMEM times an MN-major shared
 // operand).  The streamed operands (Q_i and dO_i, or K_j and V_j) flow
-// through a TMA ring.  Warps 0-3 turn S, dP into P, dS (one TMEM
-// lane, i.e. one key or one query row, per thread), warp 4 is the TMA
-// producer, warp 5 allocates TMEM.  In the dK/dV kernel warps 5 and 6
-// issue the MMAs in turns, one per half-tile buffer; in the dQ kernel warp 5
-// issues them alone.  Every wait is bounded (the device watchdog of the
-// forward kernel).
+// through a TMA ring.  Two warpgroups turn S, dP into P, dS (one TMEM lane,
+// i.e. one key or one query row, per thread), each on half of a tile's
+// columns: warps 0-3 and 7-10 in the dK/dV kernel, 0-3 and 6-9 in the dQ
+// kernel.  Warp 4 is the TMA producer, warp 5 allocates TMEM.  In the dK/dV
+// kernel warps 5 and 6 issue the MMAs in turns, one per half-tile buffer; in
+// the dQ kernel warp 5 issues them alone.  Every wait is bounded (the device
+// watchdog of the forward kernel).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -35,14 +36,20 @@ namespace fa {
 namespace {
 
 constexpr int kT = kTcRows;          // 128 rows / keys per tile
-constexpr int kBwdThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
-// dK/dV kernel: a second MMA issuer warp (see its MMA role)
-constexpr int kDkThreads = 224;
+// dQ kernel: two dS warpgroups, warps 0-3 for keys 0-63 of each tile and
+// warps 6-9 for keys 64-127 (warp w reads TMEM lanes 32 (w % 4) ..)
+constexpr int kDqThreads = 320;
+constexpr int kDqEwB = 6;
+// dK/dV kernel: a second MMA issuer warp (see its MMA role) and a second
+// elementwise warpgroup: warps 0-3 take query columns 0-31 of each half,
+// warps 7-10 columns 32-63 (warp w reads TMEM lanes 32 (w % 4) ..)
+constexpr int kDkThreads = 352;
 constexpr int kDkMmaWarpA = 5;      // issuer of half-tile buffer 0; allocates TMEM
 constexpr int kDkMmaWarpB = 6;      // issuer of half-tile buffer 1
-constexpr uint32_t kDkToken = 2;    // named barriers 2, 3 (1 is the elementwise warps')
+constexpr int kDkEwB = 7;           // first warp of the second elementwise warpgroup
+constexpr uint32_t kDkToken = 2;    // named barriers 2, 3 (1 and 4 are the elementwise warpgroups')
 constexpr uint32_t kTmemCols = 512;
 
 struct BwdTcParams {
@@ -315,13 +322,15 @@ __device__ __forceinline__ void issue_st_half(uint32_t d_tmem, uint64_t da, uint
 
 // acc (TMEM, 128 x D fp32) (+)= A (TMEM, 128 x 64 bf16) * B_x with B_x a
 // half-tile viewed MN-major (64 x D; boxes 8 KB apart): 4 MMAs of 16 rows.
+// A's queries 32 c .. 32 c + 31 (bf16 pairs) sit at columns 32 c .. 32 c + 15,
+// over the score columns that elementwise warpgroup c has read.
 template <int D>
 __device__ __forceinline__ void issue_acc_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
                                                uint32_t accumulate) {
     constexpr uint32_t idesc = idesc_bf16(kTcRows, D, 1);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, db + (uint64_t)((kk * 2048) >> 4), idesc,
+        mma_ts(d_tmem, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8, db + (uint64_t)((kk * 2048) >> 4), idesc,
                (kk > 0 || accumulate) ? 1u : 0u);
 }
 
@@ -358,10 +367,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(b.s_full + 8 * x, 1);
-            mbar_init(b.p_full + 8 * x, 4);
+            mbar_init(b.p_full + 8 * x, 8);   // both elementwise warpgroups
         }
         mbar_init(b.o_final, 2);       // one commit per issuer
-        mbar_init(b.acc_free, 4);
+        mbar_init(b.acc_free, 8);
         mbar_init(b.drain, 2);
         fence_barrier_init();
         *abort_flag = 0;
@@ -515,8 +524,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_drain(b.drain, 0, p.wait_limit_ns);
     } else {
         // ---------------------------------------------- P^T and dS^T
-        const int r = warp * 32 + lane;           // key within the block (TMEM lane)
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // Two warpgroups: cw = 0 (warps 0-3) takes the queries 0-31 of each
+        // half, cw = 1 (warps 7-10) the queries 32-63; both cover all keys.
+        const int cw = warp < kDkEwB ? 0 : 1;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;        // key within the block (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off;
         const uint32_t t_dv = t_s + 2 * kT, t_dk = t_dv + D;
         const float c = p.scale_log2;
@@ -530,27 +543,27 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             dk_rows<WIN>(p, j0, n, i_first, halves);
             const float *L = p.lse + sq.stat0;
             const float *Dl = p.delta + sq.stat0;
-            // threads 0..63 stage the row statistics of query r of each half,
-            // loaded one half ahead
-            int iq = i_first + r;
+            // lanes 0..31 of the quarter-0 warp stage the row statistics of
+            // query 32 cw + r of each half, loaded one half ahead
+            int iq = i_first + 32 * cw + r;
             float nl = 0.f, nd = 0.f;
-            if (r < 64) {
+            if (r < 32) {
                 nl = iq < n ? L[iq] * kLog2e : INFINITY;
                 nd = iq < n ? Dl[iq] : 0.f;
             }
             for (int u = 0; u < halves; ++u) {
                 const int gu = g + u, x = u & 1;
                 float *sl = stat + x * 2 * 64, *sd = sl + 64;
-                if (r < 64) {
-                    sl[r] = nl;
-                    sd[r] = nd;
+                if (r < 32) {
+                    sl[32 * cw + r] = nl;
+                    sd[32 * cw + r] = nd;
                     iq += 64;
                     if (u + 1 < halves) {
                         nl = iq < n ? L[iq] * kLog2e : INFINITY;
                         nd = iq < n ? Dl[iq] : 0.f;
                     }
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                named_bar_sync(cw == 0 ? 1u : 4u, 128);   // this warpgroup's statistics staged
                 const uint32_t t_st = t_s + x * 2 * 64, t_dpt = t_st + 64;
                 if (!warp_wait(b.s_full + 8 * x, (gu >> 1) & 1, wc, 0x60)) { ok = false; break; }
                 tc_fence_after();
@@ -569,8 +582,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     qmin = r - x * 64;
                     qmax = 63;
                 }
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                {
+                    const int cc = cw;
                     float sv[32], dpv[32];
                     tmem_ld32(t_st + cc * 32, sv);
                     tmem_ld32(t_dpt + cc * 32, dpv);
@@ -600,8 +613,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         dk[e / 2] = pack_bf16x2(g0.x, g0.y);
                         dk[e / 2 + 1] = pack_bf16x2(g1.x, g1.y);
                     }
-                    tmem_st16(t_st + cc * 16, pk);    // P^T over S^T columns already read
-                    tmem_st16(t_dpt + cc * 16, dk);   // dS^T over dP^T columns already read
+                    tmem_st16(t_st + cc * 32, pk);    // P^T over S^T columns this warpgroup has read
+                    tmem_st16(t_dpt + cc * 32, dk);   // dS^T over dP^T columns this warpgroup has read
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -614,15 +627,16 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             const int key = j0 + r;
             Tout *dV = static_cast<Tout *>(p.dv) + sq.elem0 + key * sq.rstride;
             Tout *dK = static_cast<Tout *>(p.dk) + sq.elem0 + key * sq.rstride;
+            // warpgroup 0 stores dV, warpgroup 1 dK
+            const uint32_t t_acc = cw == 0 ? t_dv : t_dk;
+            Tout *const dst = cw == 0 ? dV : dK;
+            const float mul = cw == 0 ? 1.f : p.scale;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float xo[32];
-                tmem_ld32(t_dv + cc * 32, xo);
+                tmem_ld32(t_acc + cc * 32, xo);
                 tmem_wait_ld();
-                if (key < n) store_row(dV + cc * 32, xo, 1.f);
-                tmem_ld32(t_dk + cc * 32, xo);
-                tmem_wait_ld();
-                if (key < n) store_row(dK + cc * 32, xo, p.scale);
+                if (key < n) store_row(dst + cc * 32, xo, mul);
             }
             // dK, dV are out of TMEM: the next item may overwrite them
             tc_fence_before();
@@ -720,8 +734,20 @@ __device__ __forceinline__ void dq_tiles(const BwdTcParams &p, int ib, int len, 
     }
 }
 
+// dQ (TMEM, 128 x D fp32) (+)= dS (TMEM, 128 x 128 bf16) * K (smem, 128 x D,
+// MN-major): as issue_pv, but dS's keys 64 c .. 64 c + 63 (bf16 pairs) sit at
+// columns 64 c .. 64 c + 31, over the score columns dS warpgroup c has read.
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t a_tmem, uint64_t dk, uint32_t accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(kTcRows, D, 1);
+#pragma unroll
+    for (int kk = 0; kk < kTcRows / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, dk + (uint64_t)((kk * 2048) >> 4), idesc,
+               (kk > 0 || accumulate) ? 1u : 0u);
+}
+
 template <int D, typename Tout, bool WIN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdTcParams p) {
@@ -753,9 +779,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(s_full, 1);
         mbar_init(s_full + 8, 1);
         mbar_init(dp_full, 1);
-        mbar_init(ds_full, 4);
+        mbar_init(ds_full, 8);   // both dS warpgroups
         mbar_init(o_final, 1);
-        mbar_init(acc_free, 4);
+        mbar_init(acc_free, 8);
         mbar_init(drain, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -896,7 +922,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_commit(kv_empty + 8 * (lvn % C::kSlots));
                         if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
                     }
-                    issue_pv<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
+                    issue_dq<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
                     mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
                     if (t + 2 < tiles) {
                         // S_{t+2} overwrites dS_t's buffer after dQ_t has read it (in order)
@@ -919,10 +945,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_drain(drain, 0, p.wait_limit_ns);
     } else {
         // ------------------------------------------------------- dS
-        const int r = warp * 32 + lane;           // query row within the block (TMEM lane)
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // Two warpgroups: cw = 0 (warps 0-3) takes keys 0-63 of each tile,
+        // cw = 1 (warps 6-9) keys 64-127; both cover all query rows.
+        const int cw = warp < kDqEwB ? 0 : 1;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;        // query row within the block (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s0 = tmem + lane_off, t_dp = t_s0 + 2 * kT, t_dq = t_s0 + 3 * kT;
         const float c = p.scale_log2;
+        constexpr int kH = kT / 2;                // keys per warpgroup
         int k = 0, it = 0, ib;
         uint32_t gt = 0;
         bool ok = true;
@@ -943,20 +974,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             for (int t = 0; t < tiles; ++t) {
                 const uint32_t g = gt + t;
-                const uint32_t t_s = t_s0 + (g & 1) * kT;
+                const uint32_t t_s = t_s0 + (g & 1) * kT + cw * kH;   // this warpgroup's keys
                 if (!warp_wait(s_full + 8 * (g & 1), (g >> 1) & 1, wc, 0x70)) { ok = false; break; }
                 tc_fence_after();
-                const int key0 = (t_lo + t) * kT;
-                const bool need_mask = key0 + kT > lim || (WIN && key0 < lim_lo);
-                // P = exp2(S c - L) for the whole row while dP may still be computed
-                float pv[kT];
+                const int key0 = (t_lo + t) * kT + cw * kH;
+                const bool need_mask = key0 + kH > lim || (WIN && key0 < lim_lo);
+                // P = exp2(S c - L) for the warpgroup's keys while dP may still be computed
+                float pv[kH];
 #pragma unroll
-                for (int cc = 0; cc < kT / 32; ++cc) tmem_ld32(t_s + cc * 32, pv + cc * 32);
+                for (int cc = 0; cc < kH / 32; ++cc) tmem_ld32(t_s + cc * 32, pv + cc * 32);
                 tmem_wait_ld();
                 const float2 c2 = make_float2(c, c), nl2 = make_float2(-lrow, -lrow);
                 const float2 nd2 = make_float2(-drow, -drow);
 #pragma unroll
-                for (int x = 0; x < kT; x += 2) {
+                for (int x = 0; x < kH; x += 2) {
                     const float2 a = __ffma2_rn(make_float2(pv[x], pv[x + 1]), c2, nl2);
                     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                     if (need_mask) {
@@ -970,9 +1001,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!warp_wait(dp_full, g & 1, wc, 0x72)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < kT / 32; ++cc) {
+                for (int cc = 0; cc < kH / 32; ++cc) {
                     float dpv[32];
-                    tmem_ld32(t_dp + cc * 32, dpv);
+                    tmem_ld32(t_dp + cw * kH + cc * 32, dpv);
                     tmem_wait_ld();
                     uint32_t dk[16];
 #pragma unroll
@@ -981,7 +1012,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float2 gg = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), nd2));
                         dk[x / 2] = pack_bf16x2(gg.x, gg.y);
                     }
-                    tmem_st16(t_s + cc * 16, dk);    // dS over S columns already read
+                    tmem_st16(t_s + cc * 16, dk);    // dS over S columns this warpgroup has read
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -991,11 +1022,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             if (!warp_wait(o_final, it & 1, wc, 0x71)) break;
             tc_fence_after();
-            Tout *dQ = static_cast<Tout *>(p.dq) + sq.elem0 + row * sq.rstride;
+            // each warpgroup stores half of the row's dQ columns
+            Tout *dQ = static_cast<Tout *>(p.dq) + sq.elem0 + row * sq.rstride + cw * (D / 2);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 float x[32];
-                tmem_ld32(t_dq + cc * 32, x);
+                tmem_ld32(t_dq + cw * (D / 2) + cc * 32, x);
                 tmem_wait_ld();
                 if (row < n) store_row(dQ + cc * 32, x, p.scale);
             }
@@ -1075,7 +1107,7 @@ fa_status launch(const FaBwdProblem &p) {
     static FaCtxSet ready;  // contexts set up for this instantiation
     const fa_status su = fa_once_per_context(ready, []() -> fa_status {
         const fa_status st = prepare(bwd_dkdv_tc_kernel<D, Tout, WIN>, DkCfg<D>::kSmemBytes, kDkThreads);
-        return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes, kBwdThreads) : st;
+        return st == FA_OK ? prepare(bwd_dq_tc_kernel<D, Tout, WIN>, DqCfg<D>::kSmemBytes, kDqThreads) : st;
     });
     if (su != FA_OK) return su;
     int grid_dk = p.grid_ctas > 0 ? p.grid_ctas : num_sms();   // persistent: one CTA per SM
@@ -1085,7 +1117,7 @@ fa_status launch(const FaBwdProblem &p) {
                                                                                          k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fa_cuda_fail(e);
-    bwd_dq_tc_kernel<D, Tout, WIN><<<grid_dk, kBwdThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
+    bwd_dq_tc_kernel<D, Tout, WIN><<<grid_dk, kDqThreads, DqCfg<D>::kSmemBytes, p.stream>>>(tq, tk, tv, tdo, k);
     e = cudaGetLastError();
     return e == cudaSuccess ? FA_OK : fa_cuda_fail(e);
 }
