@@ -23,8 +23,9 @@
 // columns: warps 0-3 and 7-10 in the dK/dV kernel, 0-3 and 6-9 in the dQ
 // kernel.  Warp 4 is the TMA producer, warp 5 allocates TMEM.  In the dK/dV
 // kernel warps 5 and 6 issue the MMAs in turns, one per half-tile buffer; in
-// the dQ kernel warp 5 issues them alone.  Every wait is bounded (the device
-// watchdog of the forward kernel).
+// the dQ kernel warp 5 issues them and warp 10 does the waits for its next
+// issue block meanwhile.  Every wait is bounded (the device watchdog of the
+// forward kernel).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -40,8 +41,12 @@ constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 // dQ kernel: two dS warpgroups, warps 0-3 for keys 0-63 of each tile and
 // warps 6-9 for keys 64-127 (warp w reads TMEM lanes 32 (w % 4) ..)
-constexpr int kDqThreads = 320;
+constexpr int kDqThreads = 352;
 constexpr int kDqEwB = 6;
+// dQ kernel: warp 10 does the MMA warp's barrier waits for the next issue
+// block while warp 5 issues the current one; they meet at named barrier 1
+constexpr int kDqWaitWarp = 10;
+constexpr uint32_t kDqGo = 1;
 // dK/dV kernel: a second MMA issuer warp (see its MMA role) and a second
 // elementwise warpgroup: warps 0-3 take query columns 0-31 of each half,
 // warps 7-10 columns 32-63 (warp w reads TMEM lanes 32 (w % 4) ..)
@@ -766,10 +771,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t acc_free = o_final + 8, drain = acc_free + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + C::kBarBytes - 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 8);
+    volatile int *stop_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + C::kBarBytes - 12);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x, G = gridDim.x;
 
     if (warp == kProdWarp && lane == 0) {
+        *stop_flag = 0;
         mbar_init(fix_full, 1);
         mbar_init(qd_free, 1);
         for (int i = 0; i < C::kSlots; ++i) {
@@ -848,8 +855,24 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             for (uint32_t u = li > (uint32_t)C::kSlots ? li - C::kSlots : 0; u < li; ++u)
                 mbar_drain(kv_full + 8 * (u % C::kSlots), (u / C::kSlots) & 1, lim);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kDqWaitWarp) {
         // --------------------------------------------------------- MMA
+        // Warp 5 issues; warp 10 runs the same walk but only waits: for each
+        // issue step it waits for that step's barriers (ring loads, dS, the
+        // previous item's dQ read) while warp 5 is still issuing the step
+        // before, then both meet at named barrier kDqGo and warp 5 issues.
+        // The waits (each costs the issuer a few hundred cycles when the dS
+        // warps of its sub-partition are busy) thus overlap the MMAs.  A
+        // wait that gives up raises the stop flag before the meeting.
+        const bool issuer = warp == kMmaWarp;
+        auto go = [&](bool waits_ok) -> bool {
+            if (!waits_ok) *stop_flag = 1;
+            __syncwarp();
+            named_bar_sync(kDqGo, 64);
+            if (*stop_flag) return false;
+            if (issuer) tc_fence_after();
+            return true;
+        };
         constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
         const uint64_t d_q = smem_desc(base, 16, 1024), d_do = d_q + kTileDesc;
         const uint64_t d_ring_k = smem_desc(ring, 16, 1024);
@@ -868,11 +891,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             // Tile t uses S buffer (gt + t) & 1.
             uint32_t cur = lb;
             const uint32_t ls0 = cur++, lv0 = cur++;
-            if (!warp_wait(fix_full, it & 1, wc, 0x54) || !ring_wait(kv_full, ls0, C::kSlots, wc, 0x55) ||
-                !ring_wait(kv_full, lv0, C::kSlots, wc, 0x55))
+            if (!go(issuer || (warp_wait(fix_full, it & 1, wc, 0x54) && ring_wait(kv_full, ls0, C::kSlots, wc, 0x55) &&
+                               ring_wait(kv_full, lv0, C::kSlots, wc, 0x55))))
                 break;
-            tc_fence_after();
-            if (elect_one()) {
+            if (issuer && elect_one()) {
                 issue_qk<D>(tmem + (gt & 1) * kT, d_q, d_ring_k + (ls0 % C::kSlots) * kTileDesc);  // S_0
                 mma_commit(s_full + 8 * (gt & 1));
                 if (C::kReloadK) mma_commit(kv_empty + 8 * (ls0 % C::kSlots));
@@ -884,9 +906,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             __syncwarp();
             if (tiles > 1) {
                 const uint32_t ls1 = cur++;
-                if (!ring_wait(kv_full, ls1, C::kSlots, wc, 0x55)) break;
-                tc_fence_after();
-                if (elect_one()) {
+                if (!go(issuer || ring_wait(kv_full, ls1, C::kSlots, wc, 0x55))) break;
+                if (issuer && elect_one()) {
                     issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + (ls1 % C::kSlots) * kTileDesc);
                     mma_commit(s_full + 8 * ((gt + 1) & 1));                                    // S_1
                     if (C::kReloadK) mma_commit(kv_empty + 8 * (ls1 % C::kSlots));
@@ -908,14 +929,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
                 // The loads first (they do not depend on the dS step), then dS_t;
                 // then one issue block: dP_{t+1}, dQ_t, S_{t+2}.
-                if (t + 1 < tiles && !ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) { ok = false; break; }
-                if (!ring_wait(kv_full, lk, C::kSlots, wc, 0x57)) { ok = false; break; }
-                if (t + 2 < tiles && !ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) { ok = false; break; }
-                if (!warp_wait(ds_full, g & 1, wc, 0x56)) { ok = false; break; }
-                // the previous item's dQ has been read out of TMEM
-                if (t == 0 && it > 0 && !warp_wait(acc_free, (it - 1) & 1, wc, 0x5a)) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
+                bool okw = true;
+                if (!issuer) {
+                    okw = (t + 1 >= tiles || ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) &&
+                          ring_wait(kv_full, lk, C::kSlots, wc, 0x57) &&
+                          (t + 2 >= tiles || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) &&
+                          warp_wait(ds_full, g & 1, wc, 0x56) &&
+                          // the previous item's dQ has been read out of TMEM
+                          (t != 0 || it == 0 || warp_wait(acc_free, (it - 1) & 1, wc, 0x5a));
+                }
+                if (!go(okw)) { ok = false; break; }
+                if (issuer && elect_one()) {
                     if (t + 1 < tiles) {
                         issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
                         mma_commit(dp_full);
@@ -934,15 +958,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 __syncwarp();
             }
             if (!ok) break;
-            if (elect_one()) mma_commit(o_final);
+            if (issuer && elect_one()) mma_commit(o_final);
             __syncwarp();
             lb = C::kReloadK ? cur : lb + 2 * tiles;
             gt += tiles;
             ++it;
         }
-        if (elect_one()) mma_commit(drain);
-        __syncwarp();
-        mbar_drain(drain, 0, p.wait_limit_ns);
+        if (issuer) {
+            // Teardown: wait for every MMA issued so far before TMEM is freed.
+            if (elect_one()) mma_commit(drain);
+            __syncwarp();
+            mbar_drain(drain, 0, p.wait_limit_ns);
+        }
     } else {
         // ------------------------------------------------------- dS
         // Two warpgroups: cw = 0 (warps 0-3) takes keys 0-63 of each tile,
