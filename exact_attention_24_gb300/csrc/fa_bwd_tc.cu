@@ -927,35 +927,46 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     lvn = lk + 3;
                     lk2 = lk + 4;
                 }
-                // The loads first (they do not depend on the dS step), then dS_t;
-                // then one issue block: dP_{t+1}, dQ_t, S_{t+2}.
+                // D = 128 (K loaded again for dQ): two issue steps.  Step 1:
+                // dP_{t+1} and dQ_t, once V_{t+1}, K_t and dS_t are in.  Step 2:
+                // S_{t+2}, once K_{t+2} is in.  K_{t+2}'s load is the block's
+                // last, into the slot that the previous block's dP freed, so
+                // waiting for it only after step 1 lets dP_{t+1} start as soon
+                // as dS_t is in.  D = 64 (ten slots, the loads long in place):
+                // one step.
+                constexpr bool kSplit = C::kReloadK;
                 bool okw = true;
                 if (!issuer) {
                     okw = (t + 1 >= tiles || ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) &&
                           ring_wait(kv_full, lk, C::kSlots, wc, 0x57) &&
-                          (t + 2 >= tiles || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) &&
+                          (kSplit || t + 2 >= tiles || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) &&
                           warp_wait(ds_full, g & 1, wc, 0x56) &&
                           // the previous item's dQ has been read out of TMEM
                           (t != 0 || it == 0 || warp_wait(acc_free, (it - 1) & 1, wc, 0x5a));
                 }
                 if (!go(okw)) { ok = false; break; }
+                if (issuer && elect_one() && t + 1 < tiles) {
+                    issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
+                    mma_commit(dp_full);
+                    mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+                    if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
+                }
+                __syncwarp();
                 if (issuer && elect_one()) {
-                    if (t + 1 < tiles) {
-                        issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
-                        mma_commit(dp_full);
-                        mma_commit(kv_empty + 8 * (lvn % C::kSlots));
-                        if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
-                    }
                     issue_dq<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
                     mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
-                    if (t + 2 < tiles) {
+                }
+                __syncwarp();
+                if (t + 2 < tiles) {
+                    if (kSplit && !go(issuer || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58))) { ok = false; break; }
+                    if (issuer && elect_one()) {
                         // S_{t+2} overwrites dS_t's buffer after dQ_t has read it (in order)
                         issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
                         mma_commit(s_full + 8 * (g & 1));
                         if (C::kReloadK) mma_commit(kv_empty + 8 * (lk2 % C::kSlots));
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             if (!ok) break;
             if (issuer && elect_one()) mma_commit(o_final);
