@@ -549,23 +549,25 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             const float *L = p.lse + sq.stat0;
             const float *Dl = p.delta + sq.stat0;
             // lanes 0..31 of the quarter-0 warp stage the row statistics of
-            // query 32 cw + r of each half, loaded one half ahead
+            // query 32 cw + r of each half, loaded one half ahead; the loaded
+            // values are first used when they are staged, so the load's latency
+            // does not hold up the warp (and with it its warpgroup's barrier)
             int iq = i_first + 32 * cw + r;
-            float nl = 0.f, nd = 0.f;
-            if (r < 32) {
-                nl = iq < n ? L[iq] * kLog2e : INFINITY;
-                nd = iq < n ? Dl[iq] : 0.f;
+            float rl = 0.f, rd = 0.f;
+            if (r < 32 && iq < n) {
+                rl = L[iq];
+                rd = Dl[iq];
             }
             for (int u = 0; u < halves; ++u) {
                 const int gu = g + u, x = u & 1;
                 float *sl = stat + x * 2 * 64, *sd = sl + 64;
                 if (r < 32) {
-                    sl[32 * cw + r] = nl;
-                    sd[32 * cw + r] = nd;
+                    sl[32 * cw + r] = iq < n ? rl * kLog2e : INFINITY;
+                    sd[32 * cw + r] = iq < n ? rd : 0.f;
                     iq += 64;
-                    if (u + 1 < halves) {
-                        nl = iq < n ? L[iq] * kLog2e : INFINITY;
-                        nd = iq < n ? Dl[iq] : 0.f;
+                    if (u + 1 < halves && iq < n) {
+                        rl = L[iq];
+                        rd = Dl[iq];
                     }
                 }
                 named_bar_sync(cw == 0 ? 1u : 4u, 128);   // this warpgroup's statistics staged
