@@ -540,23 +540,41 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const float c = p.scale_log2;
         int k = 0, it = 0, g = 0;
         bool ok = true;
+        // lanes 0..31 of the quarter-0 warp stage the row statistics of
+        // query 32 cw + r of each half, loaded one half ahead (across items:
+        // the next item's first half during the current item's last); the
+        // loaded values are first used when they are staged, so the load's
+        // latency does not hold up the warp (and with it its warpgroup's
+        // barrier)
         Seq sq;
         int j0;
-        while (ok && next_dk_item(p, sched, k, cta, G, D, sq, j0)) {
+        bool have = next_dk_item(p, sched, k, cta, G, D, sq, j0);
+        float rl = 0.f, rd = 0.f;
+        if (have && r < 32) {
+            int i_f, hv;
+            dk_rows<WIN>(p, j0, sq.len, i_f, hv);
+            const int iq0 = i_f + 32 * cw + r;
+            if (iq0 < sq.len) {
+                rl = p.lse[sq.stat0 + iq0];
+                rd = p.delta[sq.stat0 + iq0];
+            }
+        }
+        while (ok && have) {
             const int n = sq.len;
             int i_first, halves;
             dk_rows<WIN>(p, j0, n, i_first, halves);
             const float *L = p.lse + sq.stat0;
             const float *Dl = p.delta + sq.stat0;
-            // lanes 0..31 of the quarter-0 warp stage the row statistics of
-            // query 32 cw + r of each half, loaded one half ahead; the loaded
-            // values are first used when they are staged, so the load's latency
-            // does not hold up the warp (and with it its warpgroup's barrier)
             int iq = i_first + 32 * cw + r;
-            float rl = 0.f, rd = 0.f;
-            if (r < 32 && iq < n) {
-                rl = L[iq];
-                rd = Dl[iq];
+            // the next item, for its first half's statistics
+            Seq sq2;
+            int j02;
+            const bool have2 = next_dk_item(p, sched, k, cta, G, D, sq2, j02);
+            int iq2 = 0;
+            if (have2) {
+                int i_f2, hv2;
+                dk_rows<WIN>(p, j02, sq2.len, i_f2, hv2);
+                iq2 = i_f2 + 32 * cw + r;
             }
             for (int u = 0; u < halves; ++u) {
                 const int gu = g + u, x = u & 1;
@@ -565,9 +583,14 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     sl[32 * cw + r] = iq < n ? rl * kLog2e : INFINITY;
                     sd[32 * cw + r] = iq < n ? rd : 0.f;
                     iq += 64;
-                    if (u + 1 < halves && iq < n) {
-                        rl = L[iq];
-                        rd = Dl[iq];
+                    if (u + 1 < halves) {
+                        if (iq < n) {
+                            rl = L[iq];
+                            rd = Dl[iq];
+                        }
+                    } else if (have2 && iq2 < sq2.len) {
+                        rl = p.lse[sq2.stat0 + iq2];
+                        rd = p.delta[sq2.stat0 + iq2];
                     }
                 }
                 named_bar_sync(cw == 0 ? 1u : 4u, 128);   // this warpgroup's statistics staged
@@ -651,6 +674,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             if (lane == 0) mbar_arrive(b.acc_free);
             g += halves;
             ++it;
+            sq = sq2;
+            j0 = j02;
+            have = have2;
         }
     }
     tc_fence_before();
