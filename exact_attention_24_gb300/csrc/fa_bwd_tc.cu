@@ -693,11 +693,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // after dP_j, K_j after dQ's use of it.  Two TMEM buffers hold S (the
 // softmax warps write dS over it), one holds dP.  Per tile t the MMA warp
 // issues, once dS_t is ready:
+//   S_{t+1} = Q K_{t+1}^T     (into dS_{t-1}'s buffer, which dQ has read)
 //   dP_{t+1} = dO V_{t+1}^T   (the dP buffer has been read)
 //   dQ += dS_t K_t
-//   S_{t+2} = Q K_{t+2}^T     (into dS_t's buffer, after dQ read it)
-// so the softmax warps' next input (S_{t+1}, computed a tile earlier, and
-// dP_{t+1}) waits for one MMA only.  Persistent like the dK/dV kernel: Q
+// so the softmax warps' next inputs come first.  Persistent like the dK/dV kernel: Q
 // and dO are reloaded once the item's last dP is issued, the next item's
 // first S, dP run during the previous epilogue, and its first dQ MMA waits
 // for that epilogue to have read dQ.
@@ -913,10 +912,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         while (ok && next_dq_item(p, sched, k, cta, G, D, sq, ib)) {
             int t_lo, tiles;
             dq_tiles<WIN>(p, ib, sq.len, t_lo, tiles);
-            // Ring loads in the producer's order: K_0 = lb, V_0 = lb + 1,
-            // K_1 = lb + 2 either way; then per tile t: V_{t+1}, K_t, K_{t+2}
-            // (kReloadK, one reader each), or K_j = lb + 2j, V_j = lb + 2j + 1.
-            // Tile t uses S buffer (gt + t) & 1.
+            // Ring loads in the producer's order: K_0 = lb, V_0 = lb + 1;
+            // then per tile t: K_{t+1}, V_{t+1}, K_t again (kReloadK, one
+            // reader each; the same sequence as the producer's K_1 | V_1, K_0,
+            // K_2 | ...), or K_j = lb + 2j, V_j = lb + 2j + 1.  Tile t uses S
+            // buffer (gt + t) & 1.
             uint32_t cur = lb;
             const uint32_t ls0 = cur++, lv0 = cur++;
             if (!go(issuer || (warp_wait(fix_full, it & 1, wc, 0x54) && ring_wait(kv_full, ls0, C::kSlots, wc, 0x55) &&
@@ -932,66 +932,92 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 if (tiles == 1) mma_commit(qd_free);                                            // Q, dO read
             }
             __syncwarp();
-            if (tiles > 1) {
-                const uint32_t ls1 = cur++;
-                if (!go(issuer || ring_wait(kv_full, ls1, C::kSlots, wc, 0x55))) break;
-                if (issuer && elect_one()) {
-                    issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + (ls1 % C::kSlots) * kTileDesc);
-                    mma_commit(s_full + 8 * ((gt + 1) & 1));                                    // S_1
-                    if (C::kReloadK) mma_commit(kv_empty + 8 * (ls1 % C::kSlots));
-                }
-                __syncwarp();
-            }
-            for (int t = 0; t < tiles; ++t) {
-                const uint32_t g = gt + t;
-                const uint32_t t_buf = tmem + (g & 1) * kT;
-                uint32_t lvn, lk, lk2;   // V_{t+1}, K_t (for dQ_t), K_{t+2}
-                if (C::kReloadK) {
-                    lvn = t + 1 < tiles ? cur++ : 0u;
-                    lk = cur++;
-                    lk2 = t + 2 < tiles ? cur++ : 0u;
-                } else {
-                    lk = lb + 2 * t;
-                    lvn = lk + 3;
-                    lk2 = lk + 4;
-                }
-                // D = 128 (K loaded again for dQ): two issue steps.  Step 1:
-                // dP_{t+1} and dQ_t, once V_{t+1}, K_t and dS_t are in.  Step 2:
-                // S_{t+2}, once K_{t+2} is in.  K_{t+2}'s load is the block's
-                // last, into the slot that the previous block's dP freed, so
-                // waiting for it only after step 1 lets dP_{t+1} start as soon
-                // as dS_t is in.  D = 64 (ten slots, the loads long in place):
-                // one step.
-                constexpr bool kSplit = C::kReloadK;
-                bool okw = true;
-                if (!issuer) {
-                    okw = (t + 1 >= tiles || ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) &&
-                          ring_wait(kv_full, lk, C::kSlots, wc, 0x57) &&
-                          (kSplit || t + 2 >= tiles || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) &&
-                          warp_wait(ds_full, g & 1, wc, 0x56) &&
-                          // the previous item's dQ has been read out of TMEM
-                          (t != 0 || it == 0 || warp_wait(acc_free, (it - 1) & 1, wc, 0x5a));
-                }
-                if (!go(okw)) { ok = false; break; }
-                if (issuer && elect_one() && t + 1 < tiles) {
-                    issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
-                    mma_commit(dp_full);
-                    mma_commit(kv_empty + 8 * (lvn % C::kSlots));
-                    if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
-                }
-                __syncwarp();
-                if (issuer && elect_one()) {
-                    issue_dq<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
-                    mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
-                }
-                __syncwarp();
-                if (t + 2 < tiles) {
-                    if (kSplit && !go(issuer || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58))) { ok = false; break; }
+            if constexpr (!C::kReloadK) {
+                // D = 64: S computed two tiles ahead.  Per tile t, once dS_t is
+                // in: dP_{t+1}, dQ_t, then S_{t+2} into dS_t's buffer (after dQ_t
+                // has read it, in order).  (The order of the D = 128 branch
+                // measured 8% slower here.)
+                if (tiles > 1) {
+                    const uint32_t ls1 = lb + 2;
+                    if (!go(issuer || ring_wait(kv_full, ls1, C::kSlots, wc, 0x55))) break;
                     if (issuer && elect_one()) {
-                        // S_{t+2} overwrites dS_t's buffer after dQ_t has read it (in order)
-                        issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
-                        mma_commit(s_full + 8 * (g & 1));
-                        if (C::kReloadK) mma_commit(kv_empty + 8 * (lk2 % C::kSlots));
+                        issue_qk<D>(tmem + ((gt + 1) & 1) * kT, d_q, d_ring_k + (ls1 % C::kSlots) * kTileDesc);
+                        mma_commit(s_full + 8 * ((gt + 1) & 1));                                // S_1
+                    }
+                    __syncwarp();
+                }
+                for (int t = 0; t < tiles; ++t) {
+                    const uint32_t g = gt + t;
+                    const uint32_t t_buf = tmem + (g & 1) * kT;
+                    const uint32_t lk = lb + 2 * t, lvn = lk + 3, lk2 = lk + 4;   // K_t, V_{t+1}, K_{t+2}
+                    bool okw = true;
+                    if (!issuer) {
+                        okw = (t + 1 >= tiles || ring_wait(kv_full, lvn, C::kSlots, wc, 0x57)) &&
+                              ring_wait(kv_full, lk, C::kSlots, wc, 0x57) &&
+                              (t + 2 >= tiles || ring_wait(kv_full, lk2, C::kSlots, wc, 0x58)) &&
+                              warp_wait(ds_full, g & 1, wc, 0x56) &&
+                              // the previous item's dQ has been read out of TMEM
+                              (t != 0 || it == 0 || warp_wait(acc_free, (it - 1) & 1, wc, 0x5a));
+                    }
+                    if (!go(okw)) { ok = false; break; }
+                    if (issuer && elect_one() && t + 1 < tiles) {
+                        issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
+                        mma_commit(dp_full);
+                        mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+                        if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
+                    }
+                    __syncwarp();
+                    if (issuer && elect_one()) {
+                        issue_dq<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
+                        mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
+                    }
+                    __syncwarp();
+                    if (t + 2 < tiles) {
+                        if (issuer && elect_one()) {
+                            issue_qk<D>(t_buf, d_q, d_ring_k + (lk2 % C::kSlots) * kTileDesc);  // S_{t+2}
+                            mma_commit(s_full + 8 * (g & 1));
+                        }
+                        __syncwarp();
+                    }
+                }
+            } else {
+                for (int t = 0; t < tiles; ++t) {
+                    const uint32_t g = gt + t;
+                    const uint32_t t_buf = tmem + (g & 1) * kT;                 // dS_t
+                    const uint32_t t_nxt = tmem + ((g + 1) & 1) * kT;           // S_{t+1}
+                    // K_{t+1} (for S_{t+1}), V_{t+1}, K_t again (for dQ_t)
+                    const uint32_t lkn = t + 1 < tiles ? cur++ : 0u;
+                    const uint32_t lvn = t + 1 < tiles ? cur++ : 0u;
+                    const uint32_t lk = cur++;
+                    // One issue block per key tile: S_{t+1}, dP_{t+1}, dQ_t.
+                    // S_{t+1} goes into the buffer that dQ_{t-1} has read (issued
+                    // before it, in order), so it needs no more than its K; the
+                    // block waits for dS_t (dP_{t+1} overwrites the dP that the dS
+                    // step read, dQ_t reads dS_t).  The three loads are the block's
+                    // share of the ring in load order, all issued a block earlier.
+                    bool okw = true;
+                    if (!issuer) {
+                        okw = (t + 1 >= tiles || (ring_wait(kv_full, lkn, C::kSlots, wc, 0x57) &&
+                                                  ring_wait(kv_full, lvn, C::kSlots, wc, 0x57))) &&
+                              ring_wait(kv_full, lk, C::kSlots, wc, 0x58) &&
+                              warp_wait(ds_full, g & 1, wc, 0x56) &&
+                              // the previous item's dQ has been read out of TMEM
+                              (t != 0 || it == 0 || warp_wait(acc_free, (it - 1) & 1, wc, 0x5a));
+                    }
+                    if (!go(okw)) { ok = false; break; }
+                    if (issuer && elect_one() && t + 1 < tiles) {
+                        issue_qk<D>(t_nxt, d_q, d_ring_k + (lkn % C::kSlots) * kTileDesc);   // S_{t+1}
+                        mma_commit(s_full + 8 * ((g + 1) & 1));
+                        mma_commit(kv_empty + 8 * (lkn % C::kSlots));
+                        issue_qk<D>(t_dp, d_do, d_ring_k + (lvn % C::kSlots) * kTileDesc);   // dP_{t+1}
+                        mma_commit(dp_full);
+                        mma_commit(kv_empty + 8 * (lvn % C::kSlots));
+                        if (t + 2 == tiles) mma_commit(qd_free);                           // Q, dO read
+                    }
+                    __syncwarp();
+                    if (issuer && elect_one()) {
+                        issue_dq<D>(t_dq, t_buf, d_ring_mn + (lk % C::kSlots) * kTileDesc, t > 0 ? 1u : 0u);
+                        mma_commit(kv_empty + 8 * (lk % C::kSlots));                           // K_t read
                     }
                     __syncwarp();
                 }
