@@ -692,11 +692,13 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // kSlots single-tile slots (loads K_0, V_0, K_1, V_1, ...), V_j released
 // after dP_j, K_j after dQ's use of it.  Two TMEM buffers hold S (the
 // softmax warps write dS over it), one holds dP.  Per tile t the MMA warp
-// issues, once dS_t is ready:
+// issues, once dS_t is ready (D = 128, causal or full):
 //   S_{t+1} = Q K_{t+1}^T     (into dS_{t-1}'s buffer, which dQ has read)
 //   dP_{t+1} = dO V_{t+1}^T   (the dP buffer has been read)
 //   dQ += dS_t K_t
-// so the softmax warps' next inputs come first.  Persistent like the dK/dV kernel: Q
+// so the softmax warps' next inputs come first.  D = 64 and the band
+// instantiation keep S two tiles ahead instead: dP_{t+1}, dQ_t, then
+// S_{t+2} into dS_t's buffer (measured faster there).  Persistent like the dK/dV kernel: Q
 // and dO are reloaded once the item's last dP is issued, the next item's
 // first S, dP run during the previous epilogue, and its first dQ MMA waits
 // for that epilogue to have read dQ.
